@@ -1,0 +1,45 @@
+// Host-side helpers shared by the entry points: status/error reporting,
+// device capability checks and launch checks.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+// Records a formatted reason for dsa_last_error() and returns `st`.
+dsa_status_t fail(dsa_status_t st, const char* fmt, ...);
+
+// DSA_OK when the current device is an sm_103 part; sets the error otherwise.
+dsa_status_t check_device();
+
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms();
+
+// Converts a pending launch error into DSA_ERR_CUDA.
+dsa_status_t check_launch(const char* what);
+
+// Raises the dynamic shared-memory limit of a kernel once per process.
+template <typename K>
+dsa_status_t allow_smem(K kernel, int bytes, bool& done) {
+  if (done) return DSA_OK;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "cudaFuncSetAttribute(%d bytes): %s", bytes, cudaGetErrorString(e));
+  done = true;
+  return DSA_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+constexpr float kNegSentinel = -1e30f;  // finite score of an empty / masked slot
+
+// bits OR-ed into the caller's device status word
+__device__ __forceinline__ void report(int32_t* dev_status, uint32_t bit) {
+  if (dev_status != nullptr) atomicOr(reinterpret_cast<unsigned int*>(dev_status), bit);
+}
+
+}  // namespace dsa

@@ -1,0 +1,179 @@
+/*
+ * dsa.h -- C ABI of libdsa, the DeepSeek-Sparse-Attention (DSA) step on one
+ * GB300 (sm_103a).
+ *
+ * The step, per attention layer and batch of query tokens:
+ *   a0  quantise the indexer query to e4m3, one fp32 scale per (token, head)
+ *   a1  lightning-indexer logits over a paged fp8 key cache
+ *         logits[t,s] = sum_h w[t,h] * ReLU(q[t,h,:] . dequant(k[s,:]))
+ *   a2  top-k of each logits row
+ *   a3  sparse MLA attention over the selected rows of a paged bf16 latent
+ *       KV cache, optionally split into KV splits
+ *   a4  online-softmax merge of the split partials
+ *
+ * Sources: vLLM PR #38476 "[Feature] TRITON_MLA_SPARSE backend for
+ * SM8x/11x/12x DSA Sparse MLA Support" (Changes 2: fp8 MQA logits, prefill and
+ * paged decode, the K scale applied to the fp32 dot; Changes 3: split-KV
+ * sparse-MLA decode, N-way online-softmax merge, single-pass path, -1e30
+ * sentinel for masked slots; Changes 4: CUDA-graph capture; Tests:
+ * clean/dirty logits; review thread: top-k after the indexer,
+ * per_token_group_quant_fp8 of the indexer q, chunked exact top-k) and the
+ * "vllm-dsa-mtp-sm80" README ("The skew fixes", item 0: the 132-byte indexer
+ * page per token, blocks addressed through the cache's block stride).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *     never allocates, frees or synchronises; every call only enqueues kernels
+ *     on `stream` (so a sequence of calls can be captured in a CUDA graph).
+ *   - Arguments are validated on the host before any launch. A bad argument
+ *     returns DSA_ERR_INVALID_ARG (or DSA_ERR_UNSUPPORTED for a valid but
+ *     unimplemented shape) and launches nothing; dsa_last_error() then holds
+ *     a one-line reason (thread-local, valid until the next call on the
+ *     thread).
+ *   - Values that only the device sees (block-table entries, top-k indices,
+ *     seq_lens) are checked in the kernels. A bad one never traps: the access
+ *     is skipped (masked / zero-filled) and the matching DSA_DEVERR_* bit is
+ *     OR-ed into *dev_status when dev_status is non-NULL.
+ *   - Every wait inside a kernel is bounded (about one second); a wait that
+ *     runs out sets DSA_DEVERR_TIMEOUT and the kernel returns.
+ *   - Request b owns query tokens [query_start_loc[b], query_start_loc[b+1]);
+ *     q_len_b is their count. seq_lens[b] counts the request's cached keys
+ *     INCLUDING its q_len_b new tokens, so query token t of request b sits at
+ *     position pos(t) = seq_lens[b] - q_len_b + (t - query_start_loc[b]) and
+ *     attends causally to keys 0..pos(t); valid(t) = pos(t) + 1.
+ *   - block_size must be a multiple of 64. Block table row b (stride
+ *     bt_stride int32 entries) maps logical block i of request b to a
+ *     physical block in [0, num_blocks).
+ *
+ * Paged cache layouts
+ *   Indexer key cache (fp8): block p starts at byte p * k_block_stride_bytes
+ *   (>= block_size * (Di + 4), a multiple of 16). Inside it: block_size rows
+ *   of Di e4m3 bytes (token-major), then block_size fp32 scales. The key of
+ *   token s is dequant(k[s,:]) = e4m3(k[s,:]) * scale[s]. With Di = 128 this
+ *   is the 132-byte-per-token page.
+ *   Latent KV cache (bf16): block p starts at element p * kv_block_stride;
+ *   inside it block_size rows of Dk bf16 (Dk = 576: 512 latent + 64 rope).
+ *   The value vector of a row is its first Dv elements.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dsa_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1, /* null pointer, negative size, inconsistent strides ... */
+  DSA_ERR_UNSUPPORTED = 2, /* not an sm_103 device, or dims outside the compiled set */
+  DSA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the *_workspace_size() figure */
+  DSA_ERR_CUDA = 4         /* a CUDA runtime call failed (launch error, ...) */
+} dsa_status_t;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define DSA_DEVERR_BLOCK_OOB 1u /* a block-table entry outside [0, num_blocks) was needed */
+#define DSA_DEVERR_INDEX_OOB 2u /* a top-k index outside [-1, valid(t)) was given */
+#define DSA_DEVERR_TIMEOUT 4u   /* a bounded wait inside a kernel ran out */
+#define DSA_DEVERR_SEQ_LEN 8u   /* seq_lens[b] < q_len_b, or larger than the block table can hold */
+
+/* One-line reason for the last non-OK status returned on this thread. */
+const char* dsa_last_error(void);
+
+/* Library version string. */
+const char* dsa_version(void);
+
+/*
+ * a0 on its own: quantise q_idx [T, Hi, Di] (bf16, token stride q_stride_t
+ * elements, contiguous heads and dims) to e4m3 codes q8 [T, Hi, Di] and fp32
+ * scales sq [T, Hi], scale = amax/448 (1 when amax == 0), code =
+ * e4m3_rn_satfinite(x / scale). dsa_indexer_logits performs the same
+ * quantisation internally; this entry point exposes it so its codes can be
+ * compared bit for bit. (vLLM PR #38476 review thread: per_token_group_quant_fp8
+ * quantises the indexer q per token group.)
+ */
+dsa_status_t dsa_quant_q(const void* q_idx, int64_t q_stride_t, int32_t T, int32_t Hi, int32_t Di, uint8_t* q8,
+                         float* sq, dsa_stream_t stream);
+
+/*
+ * a0 + a1: indexer logits over the paged fp8 key cache.
+ *   q_idx  bf16 [T, Hi, Di], token stride q_stride_t elements
+ *   w      fp32 [T, Hi] head weights
+ *   logits fp32 [T, ld] output. For every token t all ld entries are
+ *          written: the logit for s < valid(t), -inf for valid(t) <= s < ld
+ *          (the clean-logits contract). ld >= max_b seq_lens[b] is required
+ *          (a longer request sets DSA_DEVERR_SEQ_LEN and is clipped to ld).
+ * max_q_len is an upper bound of q_len_b over the batch (1 or 2 for decode,
+ * larger for prefill). Supported: Hi <= 64, Di in {32, 64, 128}.
+ * (vLLM PR #38476 Changes 2.)
+ */
+dsa_status_t dsa_indexer_logits(const void* q_idx, int64_t q_stride_t, const float* w, const uint8_t* k_cache,
+                                int64_t k_block_stride_bytes, int32_t num_blocks, const int32_t* block_table,
+                                int32_t bt_stride, const int32_t* seq_lens, const int32_t* query_start_loc, int32_t B,
+                                int32_t T, int32_t Hi, int32_t Di, int32_t block_size, int32_t max_q_len,
+                                float* logits, int64_t ld, int32_t* dev_status, dsa_stream_t stream);
+
+/*
+ * a2: top-k of each logits row.
+ * Row t ranks logits[t, 0:valid(t)] (fp32, compared as floats so -0.0 equals
+ * +0.0); the n = min(index_topk, valid(t)) largest are selected, equal values
+ * resolved toward the lower position. topk_idx [T, index_topk] receives the n
+ * selected positions in ascending position order, then -1 in the remaining
+ * slots. Rows longer than the single-pass limit are selected in two exact
+ * stages (per-chunk top-k, then top-k of the candidates), which needs
+ * `workspace` of dsa_topk_workspace_size() bytes (may be NULL when that is 0).
+ * (vLLM PR #38476 review thread: index_topk selection; chunked exact top-k.)
+ */
+size_t dsa_topk_workspace_size(int32_t T, int64_t ld, int32_t index_topk);
+dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* query_start_loc,
+                      int32_t B, int32_t T, int32_t index_topk, int32_t* topk_idx, void* workspace, size_t ws_bytes,
+                      dsa_stream_t stream);
+
+/*
+ * a3 (+ a4): sparse MLA decode with split-KV.
+ *   q         bf16 [T, H, Dk] (contiguous)
+ *   kv_cache  bf16 paged latent cache (layout above)
+ *   topk_idx  int32 [T, index_topk]: logical key positions of the token's
+ *             request, -1 = empty slot. An index outside [-1, valid(t)) is
+ *             treated as empty and sets DSA_DEVERR_INDEX_OOB.
+ *   out       bf16 [T, H, Dv]: softmax(scale * q . kv[sel]) @ kv[sel, :Dv]
+ *   lse       fp32 [T, H] natural-log sum-exp of the scaled scores, or NULL.
+ * num_kv_splits: 0 = pick automatically, else 1..32. With S > 1 the top-k
+ * slots are cut into S contiguous ranges of ceil(index_topk / S); each split
+ * writes fp32 partials to `workspace` (sparse_mla_workspace_size bytes) and a
+ * merge kernel combines them. Empty slots score the finite sentinel -1e30 and
+ * carry weight 0, so an all-empty split contributes nothing and no NaN
+ * appears; a token with no selected row gets out = 0 and lse = -inf.
+ * Supported: H <= 128, (Dk, Dv) in {(576, 512), (80, 64)}.
+ * (vLLM PR #38476 Changes 3.)
+ */
+size_t sparse_mla_workspace_size(int32_t T, int32_t H, int32_t Dv, int32_t num_kv_splits);
+int32_t sparse_mla_auto_splits(int32_t T, int32_t H, int32_t Dv, int32_t index_topk);
+dsa_status_t sparse_mla_decode(const void* q, const void* kv_cache, int64_t kv_block_stride, int32_t num_blocks,
+                               const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                               const int32_t* query_start_loc, const int32_t* topk_idx, int32_t B, int32_t T,
+                               int32_t H, int32_t Dk, int32_t Dv, int32_t index_topk, int32_t block_size,
+                               float softmax_scale, int32_t num_kv_splits, void* out, float* lse, void* workspace,
+                               size_t ws_bytes, int32_t* dev_status, dsa_stream_t stream);
+
+/*
+ * a3 for prefill / many query tokens: the single-pass path (no splits, no
+ * workspace). Same arguments and results as sparse_mla_decode with
+ * num_kv_splits = 1. (vLLM PR #38476 Changes 3, single-pass path.)
+ */
+dsa_status_t sparse_mla_prefill(const void* q, const void* kv_cache, int64_t kv_block_stride, int32_t num_blocks,
+                                const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                const int32_t* query_start_loc, const int32_t* topk_idx, int32_t B, int32_t T,
+                                int32_t H, int32_t Dk, int32_t Dv, int32_t index_topk, int32_t block_size,
+                                float softmax_scale, void* out, float* lse, int32_t* dev_status,
+                                dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

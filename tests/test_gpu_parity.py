@@ -1,0 +1,157 @@
+"""GPU-vs-oracle parity of every step, through the C ABI (GB300 only)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import dsa_oracle as O
+from deepseek_sparse_attention_fp8_gb300.inputs import bf16_bits_to_float, make_workload
+
+from dsa_testlib import (check_attention, check_logits, check_topk_sets, oracle_attention, oracle_logits,
+                         oracle_q_quant)
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from deepseek_sparse_attention_fp8_gb300 import api
+    from deepseek_sparse_attention_fp8_gb300.step import DsaStep
+
+# Small cases the oracle finishes in seconds, spanning several tiles and a
+# ragged tail: (workload, overrides)
+SMALL = {
+    "tiny": ("tiny", {}),
+    "decode_small": ("decode_b32_l8192", dict(B=3, lens=[1000, 2500, 777], index_topk=2048)),
+    "decode_topk_small": ("decode_b32_l8192", dict(lens=[300, 129, 64, 4000], index_topk=256)),
+    "mtp2_small": ("mixed_b64_mtp2", dict(lens=[1500, 2049, 3000, 65], index_topk=2048)),
+    "prefill_small": ("prefill_4096_of_65536", dict(L=2300, q_len=260, index_topk=512)),
+}
+
+
+def _wl(name):
+    base, kw = SMALL[name]
+    return make_workload(base, **kw)
+
+
+@pytest.fixture(scope="module", params=sorted(SMALL))
+def run_small(request):
+    wl = _wl(request.param)
+    step = DsaStep(wl)
+    step.logits.fill_(float("nan"))  # dirty buffer: every entry must be rewritten
+    step.run()
+    torch.cuda.synchronize()
+    return wl, step
+
+
+def test_quant_q_bit_exact():
+    for name in ("tiny", "decode_small"):
+        wl = _wl(name)
+        step = DsaStep(wl)
+        q8, sq = api.dsa_quant_q(step.q_idx)
+        codes, scales = oracle_q_quant(wl)
+        assert np.array_equal(q8.cpu().numpy(), codes)
+        assert np.array_equal(sq.cpu().numpy().view(np.uint32), scales.view(np.uint32))
+
+
+def test_indexer_logits(run_small):
+    wl, step = run_small
+    got = step.logits.cpu().numpy()
+    ref = oracle_logits(wl)
+    check_logits(got, ref, range(wl.T))
+    assert int(step.dev_status.item()) == 0
+
+
+def test_topk_exact_on_same_logits(run_small):
+    wl, step = run_small
+    logits = step.logits.cpu().numpy()
+    got = step.topk_idx.cpu().numpy()
+    ref = O.topk(logits, wl.seq_lens, wl.query_start_loc, wl.index_topk)
+    check_topk_sets(got, ref, range(wl.T))
+    # the library lists positions in ascending order
+    for t in range(wl.T):
+        g = got[t][got[t] >= 0]
+        assert np.all(np.diff(g) > 0)
+
+
+def test_attention(run_small):
+    wl, step = run_small
+    idx = step.topk_idx.cpu().numpy()
+    ref, ref_lse = oracle_attention(wl, idx)
+    got = step.out.float().cpu().numpy()
+    check_attention(got, ref, np.arange(wl.T), step.lse.cpu().numpy(), ref_lse)
+
+
+def test_topk_ties_and_signed_zero():
+    """Integer-valued logits with many ties, and -0.0/+0.0 ties, against a full sort."""
+    T, ld, K = 6, 5000, 700
+    rng = np.random.default_rng(3)
+    vals = rng.integers(-3, 4, (T, ld)).astype(np.float32)
+    vals[rng.random((T, ld)) < 0.3] = -0.0
+    seq = np.array([5000, 4000, 1000, 700, 699, 3], np.int32)
+    qsl = np.arange(T + 1, dtype=np.int32)
+    dev = torch.from_numpy(vals).cuda()
+    got = api.dsa_topk(dev, torch.from_numpy(seq).cuda(), torch.from_numpy(qsl).cuda(), K).cpu().numpy()
+    ref = O.topk(vals, seq, qsl, K)
+    check_topk_sets(got, ref, range(T))
+
+
+@pytest.mark.parametrize("ld", [40000, 131072])
+def test_topk_two_stage_matches_full_sort(ld):
+    T, K = 3, 2048
+    rng = np.random.default_rng(ld)
+    vals = rng.integers(-50, 50, (T, ld)).astype(np.float32)
+    seq = np.array([ld, ld - 12345, 3000], np.int32)
+    qsl = np.arange(T + 1, dtype=np.int32)
+    assert api.dsa_topk_workspace_size(T, ld, K) > 0
+    got = api.dsa_topk(torch.from_numpy(vals).cuda(), torch.from_numpy(seq).cuda(), torch.from_numpy(qsl).cuda(),
+                       K).cpu().numpy()
+    ref = O.topk(vals, seq, qsl, K)
+    check_topk_sets(got, ref, range(T))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 8, 32])
+def test_attention_splits(splits):
+    wl = _wl("decode_small")
+    step = DsaStep(wl, num_kv_splits=splits)
+    step.run()
+    idx = step.topk_idx.cpu().numpy()
+    ref, ref_lse = oracle_attention(wl, idx)
+    check_attention(step.out.float().cpu().numpy(), ref, np.arange(wl.T), step.lse.cpu().numpy(), ref_lse)
+
+
+def test_attention_empty_and_invalid_selection():
+    wl = _wl("decode_small")
+    step = DsaStep(wl, num_kv_splits=4)
+    step.run()
+    idx = step.topk_idx.clone()
+    idx[0] = -1  # token 0: nothing selected -> out 0, lse -inf
+    idx[1, :5] = torch.tensor([10**6, -7, 3, 3, 2499], dtype=torch.int32)  # out of range entries are skipped
+    step.topk_idx.copy_(idx)
+    step.dev_status.zero_()
+    for splits in (1, 4):
+        step.splits = splits
+        step.attention()
+        torch.cuda.synchronize()
+        out = step.out.float().cpu().numpy()
+        lse = step.lse.cpu().numpy()
+        assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
+        st = int(step.dev_status.item())
+        assert st & api.DSA_DEVERR_INDEX_OOB
+        host_idx = idx.cpu().numpy()
+        clean = host_idx.copy()
+        clean[1][(clean[1] < -1) | (clean[1] >= 2500)] = -1
+        ref, _ = oracle_attention(wl, clean, rows=[1])
+        check_attention(out, ref, np.array([1]))
+
+
+def test_bad_block_ids_are_masked_and_reported():
+    wl = _wl("decode_small")
+    step = DsaStep(wl)
+    bt = step.block_table.clone()
+    bt[0, 2] = wl.num_blocks + 5  # logical block 2 of request 0 -> out of range
+    step.block_table.copy_(bt)
+    step.dev_status.zero_()
+    step.indexer()
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) & api.DSA_DEVERR_BLOCK_OOB
+    lg = step.logits.cpu().numpy()
+    assert np.all(np.isneginf(lg[0, 128:192]))  # keys of the bad block
+    assert np.all(np.isfinite(lg[0, :128]))
