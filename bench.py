@@ -1,0 +1,372 @@
+"""Benchmark of one DSA step (indexer logits -> top-k -> sparse MLA + merge).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--splits S]
+
+Default workload: decode_b32_l8192 (32 requests x 1 query token, 8192 cached
+tokens each, 64x128 fp8 indexer, top-2048, 128-head 576/512 MLA). Prints one
+JSON line. `value` is decode tokens/s over the device-timed step with inputs
+resident in HBM and L2 flushed between steps; `e2e` repeats it through the
+public API with per-step inputs copied from pinned host memory and the output
+read back. Under torchrun every rank runs an independent replica (the step
+has no exchange), ranks are timed with a barrier and the max is taken.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-MLA decode tokens/s + indexer/attention HBM GB/s vs roofline (1 GB300)"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_b32_l8192")
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clock-load", action="store_true", help="skip the one-second load before the timed steps")
+    return ap.parse_args()
+
+
+def dist_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def algorithmic_bytes(wl, topk_idx_host=None):
+    """Bytes each kernel must move at minimum (the design doc lists the formulas)."""
+    T, ld, K = wl.T, wl.ld, wl.index_topk
+    qsl = wl.query_start_loc
+    valid = []
+    for b in range(wl.B):
+        ql = qsl[b + 1] - qsl[b]
+        for i in range(ql):
+            valid.append(int(wl.seq_lens[b]) - ql + i + 1)
+    valid = np.array(valid, dtype=np.int64)
+    key_bytes = int(np.sum(wl.seq_lens.astype(np.int64))) * (wl.Di + 4)
+    indexer = key_bytes + T * wl.Hi * wl.Di * 2 + T * wl.Hi * 4 + T * ld * 4
+    topk = int(np.sum(valid)) * 4 + T * K * 4
+    live = np.minimum(valid, K) if topk_idx_host is None else np.sum(topk_idx_host >= 0, axis=1)
+    attention = int(np.sum(live)) * wl.Dk * 2 + T * wl.H * wl.Dk * 2 + T * wl.H * wl.Dv * 2 + T * K * 4 + T * wl.H * 4
+    flops_att = int(np.sum(live)) * wl.H * (2 * wl.Dk + 2 * wl.Dv)
+    flops_idx = int(np.sum(valid)) * wl.Hi * wl.Di * 2
+    return dict(indexer=indexer, topk=topk, attention=attention, flops_attention=flops_att, flops_indexer=flops_idx)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            hbm = d.get("hbm_gbs") or d.get("hbm_GBs")
+            return float(hbm), "measured", d
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback", None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        out_dir = os.path.join(ROOT, "gpurun_out")
+        os.makedirs(out_dir, exist_ok=True)
+        self.path = os.path.join(out_dir, f"clocks_rank{self.gpu}.csv")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_step(wl, rows, kv_float=None, q_float=None):
+    """The oracle's DSA step for the given query rows; returns seconds."""
+    from oracle import dsa_oracle as O
+    from deepseek_sparse_attention_fp8_gb300.inputs import bf16_bits_to_float
+
+    q_float = bf16_bits_to_float(wl.q) if q_float is None else q_float
+    kv_float = bf16_bits_to_float(wl.kv_cache) if kv_float is None else kv_float
+    t0 = time.perf_counter()
+    codes, scales = O.quantize_groups(bf16_bits_to_float(wl.q_idx[rows]))
+    full_codes = np.zeros(wl.q_idx.shape, np.uint8)
+    full_scales = np.ones(wl.q_idx.shape[:2], np.float32)
+    full_codes[rows], full_scales[rows] = codes, scales
+    logits = O.indexer_logits(full_codes, full_scales, wl.w, wl.k_cache, wl.k_block_stride, wl.block_table,
+                              wl.seq_lens, wl.query_start_loc, wl.block_size, wl.ld, rows=rows)
+    idx = O.topk(logits, wl.seq_lens, wl.query_start_loc, wl.index_topk, rows=rows)
+    O.sparse_mla(q_float, kv_float, wl.kv_block_stride, wl.block_table, wl.seq_lens, wl.query_start_loc, idx,
+                 wl.softmax_scale, wl.Dv, wl.block_size, rows=rows)
+    return time.perf_counter() - t0
+
+
+def blas_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def run_reference(args, wl):
+    """The oracle timed on the host cores: each step is a bounded sample of
+    query tokens of the workload (sized so the whole run stays within a few
+    minutes), scaled to tokens/s."""
+    from deepseek_sparse_attention_fp8_gb300.inputs import bf16_bits_to_float
+
+    q_float = bf16_bits_to_float(wl.q)
+    kv_float = bf16_bits_to_float(wl.kv_cache)
+    per_tok = cpu_oracle_step(wl, [0], kv_float, q_float)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(wl.T, budget // max(per_tok, 1e-6))))
+    rows = list(range(n))
+    for _ in range(args.warmup):
+        cpu_oracle_step(wl, rows, kv_float, q_float)
+    times = [cpu_oracle_step(wl, rows, kv_float, q_float) for _ in range(args.steps)]
+    sec = float(np.mean(times))
+    value = n / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3 * wl.T / n, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "context": int(wl.seq_lens.max()),
+                       "index_topk": wl.index_topk, "H": wl.H},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": f"{n} of {wl.T} query tokens per step (full indexer row, top-k, "
+                                       f"128-head attention), numpy float64"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_info()
+    from deepseek_sparse_attention_fp8_gb300.inputs import make_workload
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, make_workload(args.workload))
+        return
+
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    from deepseek_sparse_attention_fp8_gb300.step import DsaStep
+
+    wl = make_workload(args.workload)
+    step = DsaStep(wl, device=f"cuda:{local}", num_kv_splits=args.splits)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=step.device)
+    flush_rd = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=step.device)
+
+    def flush_l2():
+        # write 256 MiB (evicts every line of the step's inputs), then read
+        # another 256 MiB so that the dirty lines are written back here and
+        # not inside the next timed step
+        flush.zero_()
+        flush_rd.sum()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) == 0, "device status bits set during warm-up"
+    assert torch.isfinite(step.out.float()).all(), "non-finite output"
+
+    # clocks: sampler runs through a one-second sustained load and the timed steps
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_end = time.time() + (0.0 if args.no_clock_load else 1.0)
+    while time.time() < t_end:
+        for _ in range(20):
+            step.run()
+        torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    barrier()
+    wall0 = time.perf_counter()
+    for k in range(K):
+        flush_l2()  # between steps: L2 holds nothing of the inputs, and nothing dirty
+        e = ev[k]
+        e[0].record(stream)
+        step.indexer()
+        e[1].record(stream)
+        step.topk()
+        e[2].record(stream)
+        step.attention()
+        e[3].record(stream)
+    barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    t_step = [ev[k][0].elapsed_time(ev[k][3]) for k in range(K)]
+    t_idx = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    t_topk = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    t_att = [ev[k][2].elapsed_time(ev[k][3]) for k in range(K)]
+    ms = float(np.mean(t_step))
+    if world > 1:
+        tt = torch.tensor([ms], device=step.device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = world * wl.T / (ms / 1e3)
+
+    # warm-L2 (no flush) for context
+    ew = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ew[0].record(stream)
+    for _ in range(20):
+        step.run()
+    ew[1].record(stream)
+    torch.cuda.synchronize()
+    ms_warm = ew[0].elapsed_time(ew[1]) / 20
+
+    # e2e through the public API with host buffers: per-step inputs (queries,
+    # head weights, block table, lengths) copied from pinned memory, output and
+    # lse read back; the caches stay resident like a serving engine's KV cache
+    e2e = None
+    if not args.no_e2e:
+        host_in = {name: getattr(step, name).cpu().pin_memory() for name in
+                   ("q_idx", "w", "q", "block_table", "seq_lens", "qsl")}
+        host_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+        host_lse = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+        Ke = max(10, min(K, 200))
+        eve = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
+        barrier()
+        for k in range(Ke):
+            flush_l2()
+            eve[k][0].record(stream)
+            for name, t in host_in.items():
+                getattr(step, name).copy_(t, non_blocking=True)
+            step.run()
+            host_out.copy_(step.out, non_blocking=True)
+            host_lse.copy_(step.lse, non_blocking=True)
+            eve[k][1].record(stream)
+        barrier()
+        ms_e2e = float(np.mean([e[0].elapsed_time(e[1]) for e in eve]))
+        if world > 1:
+            tt = torch.tensor([ms_e2e], device=step.device)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            ms_e2e = float(tt.item())
+        e2e = {"value": world * wl.T / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e}
+
+    alg = algorithmic_bytes(wl, step.topk_idx.cpu().numpy())
+    peak, peak_kind, _ = load_peaks()
+    kern = {
+        "indexer_logits": {"ms": float(np.mean(t_idx)), "bytes": alg["indexer"]},
+        "topk": {"ms": float(np.mean(t_topk)), "bytes": alg["topk"]},
+        "sparse_mla_decode": {"ms": float(np.mean(t_att)), "bytes": alg["attention"],
+                              "flops": alg["flops_attention"]},
+    }
+    for k_, v in kern.items():
+        v["GBps"] = v["bytes"] / (v["ms"] / 1e3) / 1e9
+        v["frac"] = v["GBps"] / peak
+    dom = max(kern, key=lambda k_: kern[k_]["ms"])
+    traffic = load_traffic(dom, wl.name)
+    step_bytes = alg["indexer"] + alg["topk"] + alg["attention"]
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3+bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "context": int(wl.seq_lens.max()),
+                   "index_topk": wl.index_topk, "Hi": wl.Hi, "Di": wl.Di, "H": wl.H, "Dk": wl.Dk, "Dv": wl.Dv,
+                   "block_size": wl.block_size, "num_kv_splits": step.splits,
+                   "l2": "flushed between steps (256 MiB write + 256 MiB read)", "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["GBps"], "peak": peak, "unit": "GB/s",
+                     "frac": kern[dom]["frac"], "peak_source": peak_kind, "traffic": traffic,
+                     "step_GBps": step_bytes / (ms / 1e3) / 1e9, "step_frac": step_bytes / (ms / 1e3) / 1e9 / peak},
+        "kernels": kern,
+        "warm_l2_ms_per_step": ms_warm,
+        "gpu_launches": step.kernel_launches() * K,
+        "clocks": clocks,
+        "wall_s": wall,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sec = cpu_oracle_step(wl, list(range(wl.T)))
+        line["cpu_baseline"] = {"value": wl.T / sec, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"one full step ({wl.T} query tokens), numpy float64 oracle, "
+                                          f"{sec:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def load_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if one exists for
+    this kernel and workload (null otherwise)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        return d.get(workload, {}).get(kernel)
+    except Exception:
+        return None
+
+
+if __name__ == "__main__":
+    main()

@@ -1,6 +1,7 @@
 // Host-side helpers shared by the entry points: status/error reporting,
 // device capability checks and launch checks.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -18,6 +19,12 @@ dsa_status_t check_device();
 
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
+
+// Encodes a tiled TMA descriptor (cuTensorMapEncodeTiled reached through the
+// runtime's driver entry point, so the library does not link libcuda).
+// dims/box are innermost first; strides_bytes has rank-1 entries.
+dsa_status_t make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle);
 
 // Converts a pending launch error into DSA_ERR_CUDA.
 dsa_status_t check_launch(const char* what);

@@ -19,6 +19,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -28,11 +29,61 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 192;       // 4 epilogue warps, 1 load warp, 1 MMA warp
+constexpr int kQuantThreads = 128;
 constexpr int kTileKeys = 128;
-constexpr int kStages = 4;
+constexpr int kMaxStages = 6;
 constexpr int kTileBytes = kTileKeys * 128;  // rows padded to 128 bytes in shared memory
 constexpr int kMaxTokensPerCta = 4;
+constexpr int kMaxTilesPerCta = 64;
+constexpr int kMaxBlocksPerCta = kMaxTilesPerCta * kTileKeys / 64 + 2;  // block_size >= 64
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// a0 for 16 consecutive dims of one (token, head) row. The row is spread
+// over an aligned group of 8 lanes (lane % 8 = 16-dim chunk, chunks past the
+// head dim hold zeros); the row amax is reduced with shuffles.
+// scale = amax/448 (1 if amax == 0); code = e4m3_rn_satfinite(x / scale).
+__device__ __forceinline__ uint4 quant_chunk16(uint4 a, uint4 b, float& scale) {
+  const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[i])), fabsf(bf16_hi(u[i]))));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+  scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint16_t p0 = cvt_e4m3x2(__fdiv_rn(bf16_lo(u[2 * i]), scale), __fdiv_rn(bf16_hi(u[2 * i]), scale));
+    const uint16_t p1 = cvt_e4m3x2(__fdiv_rn(bf16_lo(u[2 * i + 1]), scale), __fdiv_rn(bf16_hi(u[2 * i + 1]), scale));
+    out[i] = static_cast<uint32_t>(p0) | (static_cast<uint32_t>(p1) << 16);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// One thread per 16-dim chunk; 8 consecutive threads per (token, head) row.
+__global__ void __launch_bounds__(kQuantThreads) quant_q_kernel(const uint16_t* q, int64_t q_stride_t, int T, int Hi,
+                                                           int Di, uint8_t* q8, float* sq) {
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = g / 8;
+  const int c = static_cast<int>(g % 8);
+  const bool row_ok = row < static_cast<int64_t>(T) * Hi;
+  const bool have = row_ok && c < Di / 16;
+  uint4 a = make_uint4(0, 0, 0, 0), b = a;
+  if (have) {
+    const int64_t t = row / Hi, h = row % Hi;
+    const uint4* src = reinterpret_cast<const uint4*>(q + t * q_stride_t + h * Di) + 2 * c;
+    a = __ldg(src);
+    b = __ldg(src + 1);
+  }
+  float scale;
+  const uint4 codes = quant_chunk16(a, b, scale);
+  if (have) reinterpret_cast<uint4*>(q8 + row * Di)[c] = codes;
+  if (row_ok && c == 0) sq[row] = scale;
+}
 
 struct IndexerParams {
   const uint16_t* q;  // bf16 bits [T, Hi, Di]
@@ -51,72 +102,41 @@ struct IndexerParams {
   int32_t hi_pad;  // heads rounded up to 16: columns per token
   int32_t tiles_per_cta;
   int32_t n_tiles;  // ceil(ld / 128)
+  int32_t stages;
   float* logits;
   int64_t ld;
   int32_t* dev_status;
 };
 
 struct SmemOffsets {
-  int k, sc, bad, q, w, total;
+  int k, sc, q, w, total;
 };
-__host__ __device__ inline SmemOffsets indexer_smem(int n_cols) {
+__host__ __device__ inline SmemOffsets indexer_smem(int n_cols, int stages) {
   SmemOffsets o;
   o.k = 0;
-  o.sc = o.k + kStages * kTileBytes;
-  o.bad = o.sc + kStages * kTileKeys * 4;
-  o.q = (o.bad + kStages * 16 + 1023) & ~1023;
+  o.sc = o.k + stages * kTileBytes;
+  o.q = (o.sc + stages * kTileKeys * 4 + 1023) & ~1023;
   o.w = o.q + n_cols * 128;
   o.total = o.w + n_cols * 4 + 1024;  // + slack for 1024-byte alignment of the base
   return o;
 }
+// two CTAs per SM: stages sized so that 2 x smem stays within 228 KB
+__host__ __device__ inline int indexer_stages(int n_cols) { return n_cols <= 64 ? 6 : (n_cols <= 128 ? 5 : 4); }
 
-__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-
-// Quantises one (token, head) row of Di bf16 values. Calls emit(chunk, uint4)
-// for every 16-code chunk and returns the fp32 scale (amax/448, 1 if amax==0).
-template <typename Emit>
-__device__ __forceinline__ float quant_row(const uint16_t* src, int Di, Emit emit) {
-  const uint4* s4 = reinterpret_cast<const uint4*>(src);
-  float amax = 0.f;
-  for (int c = 0; c < Di / 8; ++c) {
-    uint4 v = __ldg(s4 + c);
-    uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[i])), fabsf(bf16_hi(u[i]))));
-  }
-  const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-  for (int c = 0; c < Di / 16; ++c) {
-    uint4 a = __ldg(s4 + 2 * c), b = __ldg(s4 + 2 * c + 1);
-    uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t out[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint16_t p0 = cvt_e4m3x2(__fdiv_rn(bf16_lo(u[2 * i]), scale), __fdiv_rn(bf16_hi(u[2 * i]), scale));
-      uint16_t p1 = cvt_e4m3x2(__fdiv_rn(bf16_lo(u[2 * i + 1]), scale), __fdiv_rn(bf16_hi(u[2 * i + 1]), scale));
-      out[i] = static_cast<uint32_t>(p0) | (static_cast<uint32_t>(p1) << 16);
-    }
-    emit(c, make_uint4(out[0], out[1], out[2], out[3]));
-  }
-  return scale;
-}
-
-__global__ void __launch_bounds__(kThreads) quant_q_kernel(const uint16_t* q, int64_t q_stride_t, int T, int Hi,
-                                                           int Di, uint8_t* q8, float* sq) {
-  const int row = blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= T * Hi) return;
-  const int t = row / Hi, h = row % Hi;
-  uint4* dst = reinterpret_cast<uint4*>(q8 + static_cast<int64_t>(row) * Di);
-  sq[row] = quant_row(q + t * q_stride_t + static_cast<int64_t>(h) * Di, Di, [&](int c, uint4 v) { dst[c] = v; });
-}
-
-__global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const IndexerParams p) {
+// Warp roles: warps 0-3 quantise the queries, then run the epilogue (warp w
+// owns TMEM lanes 32w..32w+31 = keys of the tile); warp 4 loads key tiles
+// (TMA for 128-byte rows, cp.async otherwise); warp 5 issues the MMAs.
+template <int DI>
+__global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __grid_constant__ IndexerParams p,
+                                                                     const __grid_constant__ CUtensorMap kmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t mma_bar;
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_holder;
   __shared__ int s_tok[kMaxTokensPerCta];
   __shared__ int s_valid[kMaxTokensPerCta];
+  __shared__ int s_blk[kMaxBlocksPerCta];
+  __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.y / p.n_tb;
@@ -140,51 +160,70 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const Index
   const int t_comp_end = min(t_end, (max_valid + kTileKeys - 1) / kTileKeys);  // tiles needing an MMA
   const int n_comp = max(0, t_comp_end - t_begin);
   const int n_cols = p.hi_pad * p.tb;  // MMA N
+  const int S = p.stages;
+  const int nbuf = 2 * n_cols <= 256 ? 2 : 1;
 
-  const SmemOffsets so = indexer_smem(n_cols);
+  const SmemOffsets so = indexer_smem(n_cols, S);
   uint8_t* sk = smem + so.k;
   float* ssc = reinterpret_cast<float*>(smem + so.sc);
-  uint32_t* sbad = reinterpret_cast<uint32_t*>(smem + so.bad);
   uint8_t* sq = smem + so.q;
   float* sw = reinterpret_cast<float*>(smem + so.w);
+
+  const int* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+  const int blk0 = t_begin * kTileKeys / p.block_size;
+  const int n_blk = n_comp > 0 ? ((t_begin + n_comp) * kTileKeys + p.block_size - 1) / p.block_size - blk0 : 0;
 
   if (tid < ntok) {
     s_tok[tid] = tok0 + tid;
     s_valid[tid] = min(static_cast<int64_t>(seq_len - q_len + (tok0 + tid - q0) + 1), cap);
   }
+  if (tid == 0) s_abort = 0;
 
   uint32_t tmem = 0;
-  const uint32_t tmem_cols = n_cols <= 32 ? 32 : (n_cols <= 64 ? 64 : (n_cols <= 128 ? 128 : 256));
+  const uint32_t acc_cols = n_cols <= 32 ? 32 : (n_cols <= 64 ? 64 : (n_cols <= 128 ? 128 : 256));
+  const uint32_t tmem_cols = acc_cols * nbuf;
   if (n_comp > 0) {
-    // zero the key stages once: columns past Di are never written by the loads
-    if (p.Di < 128) {
-      for (int i = tid; i < kStages * kTileBytes / 16; i += kThreads)
-        reinterpret_cast<uint4*>(sk)[i] = make_uint4(0, 0, 0, 0);
+    if constexpr (DI < 128) {  // row padding past Di is never written by the loads
+      for (int i = tid; i < S * kTileBytes / 16; i += kThreads) reinterpret_cast<uint4*>(sk)[i] = make_uint4(0, 0, 0, 0);
     }
-    // a0: quantise the token block's queries into the B operand (N rows x 128 B)
-    for (int n = tid; n < n_cols; n += kThreads) {
-      const int j = n / p.hi_pad, h = n % p.hi_pad;
-      uint8_t* row = sq;
-      if (j < ntok && h < p.Hi) {
-        const int tok = tok0 + j;
-        const float scale = quant_row(p.q + tok * p.q_stride_t + static_cast<int64_t>(h) * p.Di, p.Di,
-                                      [&](int c, uint4 v) {
-                                        *reinterpret_cast<uint4*>(row + sw128_offset(n, c)) = v;
-                                      });
-        for (int c = p.Di / 16; c < 8; ++c) *reinterpret_cast<uint4*>(row + sw128_offset(n, c)) = make_uint4(0, 0, 0, 0);
-        sw[n] = __ldg(p.w + static_cast<int64_t>(tok) * p.Hi + h) * scale;
-      } else {
-        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(row + sw128_offset(n, c)) = make_uint4(0, 0, 0, 0);
-        sw[n] = 0.f;
+    if (warp < 4) {
+      // a0: quantise the token block's queries into the B operand (N rows x 128 B)
+      for (int base = 0; base < n_cols; base += 128 / 8) {
+        const int n = base + tid / 8, c = tid % 8;
+        const int j = n / p.hi_pad, h = n % p.hi_pad;
+        const bool row_ok = j < ntok && h < p.Hi;
+        uint4 a = make_uint4(0, 0, 0, 0), bq = a;
+        if (row_ok && c < DI / 16) {
+          const uint4* src =
+              reinterpret_cast<const uint4*>(p.q + (tok0 + j) * p.q_stride_t + static_cast<int64_t>(h) * DI) + 2 * c;
+          a = __ldg(src);
+          bq = __ldg(src + 1);
+        }
+        float scale;
+        const uint4 codes = quant_chunk16(a, bq, scale);
+        *reinterpret_cast<uint4*>(sq + sw128_offset(n, c)) = codes;
+        if (c == 0) sw[n] = row_ok ? __ldg(p.w + static_cast<int64_t>(tok0 + j) * p.Hi + h) * scale : 0.f;
       }
     }
+    // block ids of every key this CTA reads
+    for (int i = tid; i < n_blk; i += kThreads) {
+      const int lb = blk0 + i;
+      s_blk[i] = lb * p.block_size < seq_len ? __ldg(bt_row + lb) : -1;
+    }
     fence_proxy_async_smem();
-    if (warp == 0) {
+    if (warp == 5) {
       tmem_alloc(&tmem_holder, tmem_cols);
       tmem_relinquish();
     }
     if (tid == 0) {
-      mbar_init(&mma_bar, 1);
+      for (int s = 0; s < S; ++s) {
+        mbar_init(&full_bar[s], DI == 128 ? 1 : 32);
+        mbar_init(&empty_bar[s], 1 + 4);
+      }
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(&acc_full[s], 1);
+        mbar_init(&acc_empty[s], 4);
+      }
       fence_mbar_init();
     }
   }
@@ -193,134 +232,166 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const Index
   tc_fence_after();
   if (n_comp > 0) tmem = tmem_holder;
 
-  const int* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-  const int chunks_per_row = p.Di / 16;
-
-  // Issues the cp.async loads of key tile `tile` into stage `st`.
-  auto load_tile = [&](int tile, int st) {
-    const int key0 = tile * kTileKeys;
-    uint8_t* dst_base = sk + st * kTileBytes;
-    const int total = kTileKeys * chunks_per_row;
-    for (int c = tid; c < total; c += kThreads) {
-      const int r = c / chunks_per_row, ch = c % chunks_per_row;
-      const int s = key0 + r;
-      const uint8_t* src = p.k_cache;
-      uint32_t bytes = 0;
-      if (s < seq_len) {
-        const int blk = __ldg(bt_row + s / p.block_size);
-        if (blk >= 0 && blk < p.num_blocks) {
-          src = p.k_cache + static_cast<int64_t>(blk) * p.k_block_stride + (s % p.block_size) * p.Di + ch * 16;
-          bytes = 16;
-        }
-      }
-      cp_async_16(smem_u32(dst_base + sw128_offset(r, ch)), src, bytes);
-    }
-    // scales: 4 consecutive keys per 16-byte chunk (block_size % 64 == 0);
-    // warp 0 loads them and records which keys sit in an out-of-range block
-    if (warp == 0) {
-      const int s = key0 + tid * 4;
-      const uint8_t* src = p.k_cache;
-      uint32_t bytes = 0;
-      bool bad = false;
-      if (s < seq_len) {
-        const int blk = __ldg(bt_row + s / p.block_size);
-        if (blk >= 0 && blk < p.num_blocks) {
-          src = p.k_cache + static_cast<int64_t>(blk) * p.k_block_stride +
-                static_cast<int64_t>(p.block_size) * p.Di + (s % p.block_size) * 4;
-          bytes = 16;
-        } else {
-          bad = true;
-        }
-      }
-      cp_async_16(smem_u32(ssc + st * kTileKeys + tid * 4), src, bytes);
-      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, bad);
-      if (lane < 4) {  // word `lane` covers keys 32*lane .. +31 = lanes 8*lane .. +7
-        uint32_t word = 0;
-        for (int k = 0; k < 8; ++k)
-          if ((bal >> (8 * lane + k)) & 1u) word |= 0xFu << (4 * k);
-        sbad[st * 4 + lane] = word;
-      }
-      if (bad) report(p.dev_status, DSA_DEVERR_BLOCK_OOB);
-    }
+  auto abort_now = [&](void) {
+    s_abort = 1;
+    report(p.dev_status, DSA_DEVERR_TIMEOUT);
+  };
+  auto block_ok = [&](int s) {  // key s < seq_len lies in a valid block
+    const int blk = s_blk[s / p.block_size - blk0];
+    return blk >= 0 && blk < p.num_blocks;
   };
 
-  const uint32_t idesc = idesc_e4m3(128, n_cols);
-  const int ksteps = p.Di / 32;
-  bool aborted = false;
-
-  // prologue: fill kStages-1 stages
-  for (int i = 0; i < kStages - 1; ++i) {
-    if (i < n_comp) load_tile(t_begin + i, i);
-    cp_async_commit();
-  }
-  for (int i = 0; i < n_comp; ++i) {
-    const int st = i % kStages;
-    // the stage refilled below was read by the previous tile's epilogue
-    if (i > 0) __syncthreads();
-    if (i + kStages - 1 < n_comp) load_tile(t_begin + i + kStages - 1, (i + kStages - 1) % kStages);
-    cp_async_commit();
-    cp_async_wait<kStages - 1>();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-      const uint32_t a0 = smem_u32(sk + st * kTileBytes), b0 = smem_u32(sq);
-      for (int ks = 0; ks < ksteps; ++ks)
-        mma_e4m3_ss(tmem, smem_desc(a0 + ks * 32, 16, 1024, kSwizzle128B), smem_desc(b0 + ks * 32, 16, 1024, kSwizzle128B),
-                    idesc, ks > 0 ? 1u : 0u);
-      mma_commit(&mma_bar);
-    }
-    __syncwarp();
-    const bool ok = mbar_wait(&mma_bar, i & 1);
-    if (__syncthreads_or(!ok)) {
-      aborted = true;
-      break;
-    }
-    tc_fence_after();
-    // epilogue: thread = key row = TMEM lane
-    const int r = warp * 32 + lane;
-    const int s = (t_begin + i) * kTileKeys + r;
-    const float scale_k = ssc[st * kTileKeys + r];
-    const bool bad = (sbad[st * 4 + (r >> 5)] >> (r & 31)) & 1u;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    for (int j = 0; j < ntok; ++j) {
-      float acc = 0.f;
-      for (int hc = 0; hc < p.hi_pad; hc += 32) {
-        if (hc + 32 <= p.hi_pad) {
-          uint32_t v[32];
-          tmem_ld32_sync(lane_addr + j * p.hi_pad + hc, v);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) acc = fmaf(sw[j * p.hi_pad + hc + x], fmaxf(__uint_as_float(v[x]), 0.f), acc);
-        } else {
-          uint32_t v[16];
-          tmem_ld16_sync(lane_addr + j * p.hi_pad + hc, v);
-#pragma unroll
-          for (int x = 0; x < 16; ++x) acc = fmaf(sw[j * p.hi_pad + hc + x], fmaxf(__uint_as_float(v[x]), 0.f), acc);
-        }
+  if (n_comp > 0 && warp == 4) {
+    // ---------------- producer
+    for (int i = 0; i < n_comp && !s_abort; ++i) {
+      const int st = i % S;
+      if (i >= S && !mbar_wait(&empty_bar[st], ((i / S) - 1) & 1)) {
+        if (lane == 0) abort_now();
+        break;
       }
-      const float out = (s < s_valid[j] && !bad) ? acc * scale_k : -INFINITY;
-      if (s < p.ld) p.logits[static_cast<int64_t>(s_tok[j]) * p.ld + s] = out;
+      const int key0 = (t_begin + i) * kTileKeys;
+      if constexpr (DI == 128) {
+        if (lane == 0) {
+          uint32_t bytes = 0;
+          int blk_u[2], off_u[2];
+          bool bad = false;
+          for (int u = 0; u < 2; ++u) {
+            const int s0 = key0 + 64 * u;
+            blk_u[u] = -1;
+            off_u[u] = s0 % p.block_size;
+            if (s0 < seq_len) {
+              if (block_ok(s0)) {
+                blk_u[u] = s_blk[s0 / p.block_size - blk0];
+                bytes += 64 * 128 + 64 * 4;
+              } else {
+                bad = true;
+              }
+            }
+          }
+          mbar_arrive_expect_tx(&full_bar[st], bytes);
+          for (int u = 0; u < 2; ++u) {
+            if (blk_u[u] < 0) continue;
+            tma_load_3d(smem_u32(sk + st * kTileBytes + u * 8192), &kmap, &full_bar[st], 0, off_u[u], blk_u[u]);
+            bulk_copy_g2s(smem_u32(ssc + st * kTileKeys + u * 64),
+                          p.k_cache + static_cast<int64_t>(blk_u[u]) * p.k_block_stride +
+                              static_cast<int64_t>(p.block_size) * 128 + off_u[u] * 4,
+                          256, &full_bar[st]);
+          }
+          if (bad) report(p.dev_status, DSA_DEVERR_BLOCK_OOB);
+        }
+      } else {
+        constexpr int kChunks = DI / 16;
+        uint8_t* dst_base = sk + st * kTileBytes;
+        for (int c = lane; c < kTileKeys * kChunks; c += 32) {
+          const int r = c / kChunks, ch = c % kChunks;
+          const int s = key0 + r;
+          const uint8_t* src = p.k_cache;
+          uint32_t bytes = 0;
+          if (s < seq_len && block_ok(s)) {
+            src = p.k_cache + static_cast<int64_t>(s_blk[s / p.block_size - blk0]) * p.k_block_stride +
+                  (s % p.block_size) * DI + ch * 16;
+            bytes = 16;
+          }
+          cp_async_16(smem_u32(dst_base + sw128_offset(r, ch)), src, bytes);
+        }
+        {  // 4 consecutive keys per 16-byte scale chunk (block_size % 64 == 0)
+          const int s = key0 + lane * 4;
+          const uint8_t* src = p.k_cache;
+          uint32_t bytes = 0;
+          if (s < seq_len) {
+            if (block_ok(s)) {
+              src = p.k_cache + static_cast<int64_t>(s_blk[s / p.block_size - blk0]) * p.k_block_stride +
+                    static_cast<int64_t>(p.block_size) * DI + (s % p.block_size) * 4;
+              bytes = 16;
+            } else {
+              report(p.dev_status, DSA_DEVERR_BLOCK_OOB);
+            }
+          }
+          cp_async_16(smem_u32(ssc + st * kTileKeys + lane * 4), src, bytes);
+        }
+        cp_async_mbar_arrive(&full_bar[st]);
+      }
     }
-    tc_fence_before();
+  } else if (n_comp > 0 && warp == 5) {
+    // ---------------- MMA issuer
+    const uint32_t idesc = idesc_e4m3(128, n_cols);
+    for (int i = 0; i < n_comp && !s_abort; ++i) {
+      const int st = i % S, buf = i % nbuf;
+      bool ok = mbar_wait(&full_bar[st], (i / S) & 1);
+      if (ok && i >= nbuf) ok = mbar_wait(&acc_empty[buf], ((i / nbuf) - 1) & 1);
+      if (!ok) {
+        if (lane == 0) abort_now();
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t a0 = smem_u32(sk + st * kTileBytes), b0 = smem_u32(sq);
+#pragma unroll
+        for (int ks = 0; ks < DI / 32; ++ks)
+          mma_e4m3_ss(tmem + buf * acc_cols, smem_desc(a0 + ks * 32, 16, 1024, kSwizzle128B),
+                      smem_desc(b0 + ks * 32, 16, 1024, kSwizzle128B), idesc, ks > 0 ? 1u : 0u);
+        mma_commit(&empty_bar[st]);
+        mma_commit(&acc_full[buf]);
+      }
+      __syncwarp();
+    }
+  } else if (n_comp > 0) {
+    // ---------------- epilogue: thread = key row = TMEM lane
+    const int r = warp * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    for (int i = 0; i < n_comp && !s_abort; ++i) {
+      const int st = i % S, buf = i % nbuf;
+      if (!mbar_wait(&acc_full[buf], (i / nbuf) & 1)) {
+        if (lane == 0) abort_now();
+        break;
+      }
+      tc_fence_after();
+      const int s = (t_begin + i) * kTileKeys + r;
+      const float scale_k = ssc[st * kTileKeys + r];
+      const bool bad = s < seq_len && !block_ok(s);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[st]);  // this warp is done with the stage's scales
+      for (int j = 0; j < ntok; ++j) {
+        float acc = 0.f;
+        const uint32_t col = buf * acc_cols + j * p.hi_pad;
+        for (int hc = 0; hc < p.hi_pad; hc += 32) {
+          if (hc + 32 <= p.hi_pad) {
+            uint32_t v[32];
+            tmem_ld32_sync(lane_addr + col + hc, v);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) acc = fmaf(sw[j * p.hi_pad + hc + x], fmaxf(__uint_as_float(v[x]), 0.f), acc);
+          } else {
+            uint32_t v[16];
+            tmem_ld16_sync(lane_addr + col + hc, v);
+#pragma unroll
+            for (int x = 0; x < 16; ++x) acc = fmaf(sw[j * p.hi_pad + hc + x], fmaxf(__uint_as_float(v[x]), 0.f), acc);
+          }
+        }
+        const float out = (s < s_valid[j] && !bad) ? acc * scale_k : -INFINITY;
+        if (s < p.ld) p.logits[static_cast<int64_t>(s_tok[j]) * p.ld + s] = out;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
   }
-  cp_async_wait<0>();
-  if (aborted && tid == 0) report(p.dev_status, DSA_DEVERR_TIMEOUT);
 
   // tiles entirely past every token's valid range: -inf only
-  for (int tile = t_begin + n_comp; tile < t_end; ++tile) {
-    const int s = tile * kTileKeys + tid;
-    if (s < p.ld)
-      for (int j = 0; j < ntok; ++j) p.logits[static_cast<int64_t>(s_tok[j]) * p.ld + s] = -INFINITY;
+  if (warp < 4) {
+    for (int tile = t_begin + n_comp; tile < t_end; ++tile) {
+      const int s = tile * kTileKeys + tid;
+      if (s < p.ld)
+        for (int j = 0; j < ntok; ++j) p.logits[static_cast<int64_t>(s_tok[j]) * p.ld + s] = -INFINITY;
+    }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (n_comp > 0 && warp == 0) tmem_dealloc(tmem, tmem_cols);
+  if (n_comp > 0 && warp == 5) tmem_dealloc(tmem, tmem_cols);
 }
 
-bool g_smem_set = false;
+bool g_smem_set[3] = {false, false, false};
 
 }  // namespace
 }  // namespace dsa
@@ -338,7 +409,8 @@ extern "C" dsa_status_t dsa_quant_q(const void* q_idx, int64_t q_stride_t, int32
   dsa_status_t st = check_device();
   if (st != DSA_OK) return st;
   const int rows = T * Hi;
-  quant_q_kernel<<<(rows + kThreads - 1) / kThreads, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+  quant_q_kernel<<<(rows * 8 + kQuantThreads - 1) / kQuantThreads, kQuantThreads, 0,
+                   reinterpret_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint16_t*>(q_idx), q_stride_t, T, Hi, Di, q8, sq);
   return check_launch("quant_q_kernel");
 }
@@ -392,15 +464,44 @@ extern "C" dsa_status_t dsa_indexer_logits(const void* q_idx, int64_t q_stride_t
   p.dev_status = dev_status;
   const int64_t rows = static_cast<int64_t>(B) * p.n_tb;
   if (rows > 65535) return fail(DSA_ERR_UNSUPPORTED, "dsa_indexer_logits: B * token blocks = %lld > 65535", (long long)rows);
-  // about four CTAs per SM in total, at least two tiles each
+  // one wave of two CTAs per SM when the work allows it, at least two tiles per CTA
+  const int64_t slots = 2LL * num_sms();
   const int64_t total_tiles = rows * p.n_tiles;
-  const int64_t target = 4LL * num_sms();
-  p.tiles_per_cta = static_cast<int32_t>(std::max<int64_t>(2, std::min<int64_t>(64, (total_tiles + target - 1) / target)));
+  int64_t tpc = std::max<int64_t>(2, (total_tiles + slots - 1) / slots);
+  while (tpc < kMaxTilesPerCta && rows * ((p.n_tiles + tpc - 1) / tpc) > slots) ++tpc;
+  p.tiles_per_cta = static_cast<int32_t>(std::min<int64_t>(tpc, kMaxTilesPerCta));
   const int n_cols = p.hi_pad * p.tb;
-  const SmemOffsets so = indexer_smem(n_cols);
-  st = allow_smem(indexer_logits_kernel, indexer_smem(256).total, g_smem_set);  // the largest N any call uses
-  if (st != DSA_OK) return st;
+  p.stages = indexer_stages(n_cols);
+  const SmemOffsets so = indexer_smem(n_cols, p.stages);
+  const int max_smem = std::max(indexer_smem(64, indexer_stages(64)).total,
+                                std::max(indexer_smem(128, indexer_stages(128)).total, indexer_smem(256, indexer_stages(256)).total));
+  CUtensorMap kmap;
+  memset(&kmap, 0, sizeof(kmap));
+  if (Di == 128) {
+    const uint64_t dims[3] = {128, static_cast<uint64_t>(block_size), static_cast<uint64_t>(std::max(num_blocks, 1))};
+    const uint64_t strides[2] = {128, static_cast<uint64_t>(k_block_stride_bytes)};
+    const uint32_t box[3] = {128, 64, 1};
+    st = make_tmap(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, k_cache, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != DSA_OK) return st;
+  }
   dim3 grid((p.n_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta, static_cast<unsigned>(rows));
-  indexer_logits_kernel<<<grid, kThreads, so.total, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (Di) {
+    case 128:
+      st = allow_smem(indexer_logits_kernel<128>, max_smem, g_smem_set[0]);
+      if (st != DSA_OK) return st;
+      indexer_logits_kernel<128><<<grid, kThreads, so.total, s>>>(p, kmap);
+      break;
+    case 64:
+      st = allow_smem(indexer_logits_kernel<64>, max_smem, g_smem_set[1]);
+      if (st != DSA_OK) return st;
+      indexer_logits_kernel<64><<<grid, kThreads, so.total, s>>>(p, kmap);
+      break;
+    default:
+      st = allow_smem(indexer_logits_kernel<32>, max_smem, g_smem_set[2]);
+      if (st != DSA_OK) return st;
+      indexer_logits_kernel<32><<<grid, kThreads, so.total, s>>>(p, kmap);
+      break;
+  }
   return check_launch("indexer_logits_kernel");
 }

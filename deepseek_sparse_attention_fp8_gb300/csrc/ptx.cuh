@@ -52,14 +52,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase with the given parity to complete. Gives up after
-// `limit_ns` nanoseconds of wall time and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = 1000000000ull) {
+// `limit_cycles` SM clock cycles (about one second at 2 GHz) and returns
+// false. The bound uses the SM cycle counter: it is cheap to read, unlike the
+// global timer, whose read latency would dominate short waits.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit_cycles = 2000000000ll) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const long long t0 = clock64();
   while (true) {
-    for (int i = 0; i < 64; ++i)
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if (clock64() - t0 > limit_cycles) return false;
   }
 }
 
@@ -89,6 +92,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
       "[%2];" ::"r"(dst),
       "l"(tmap), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
+}
+// Four rows (arbitrary row coordinates r0..r3) of a 2-D tensor, `col` onwards
+// for the box width; the box of the tensor map is one row high.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, uint64_t* bar, int32_t col, int32_t r0,
+                                            int32_t r1, int32_t r2, int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
+      "%5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(tmap), "r"(smem_u32(bar)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+      : "memory");
+}
+// Contiguous global->shared bulk copy (both addresses 16-byte aligned, size a
+// multiple of 16).
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");

@@ -33,39 +33,44 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 128;
-constexpr int kTileKeys = 64;
+constexpr int kThreads = 288;  // warps 0-3 softmax/epilogue, warps 4-7 loads, warp 8 MMA
+constexpr int kMmaWarp = 8;
+constexpr int kTileKeys = 32;
+constexpr int kStages = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
+constexpr int kMaxSlots = 4096;           // top-k slots one CTA (one split) may cover
 
 template <int DK, int DV>
 struct MlaCfg;
 template <>
 struct MlaCfg<576, 512> {
-  static constexpr int kDvSplit = 2, kDvc = 256, kDkTmem = 384, kNkb = 9, kQsmKb = 3, kStages = 2, kTmemCols = 512;
+  static constexpr int kDvSplit = 2, kDvc = 256, kDkTmem = 448, kNkb = 9, kTmemCols = 512;
 };
 template <>
 struct MlaCfg<80, 64> {
-  static constexpr int kDvSplit = 1, kDvc = 64, kDkTmem = 64, kNkb = 2, kQsmKb = 1, kStages = 2, kTmemCols = 256;
+  static constexpr int kDvSplit = 1, kDvc = 64, kDkTmem = 64, kNkb = 2, kTmemCols = 128;
 };
 
 template <int DK, int DV>
 struct MlaSmem {
   using C = MlaCfg<DK, DV>;
+  static constexpr int kQsmKb = C::kNkb - C::kDkTmem / 64;  // q K-blocks read from shared memory
+  static constexpr int kKvKb = kTileKeys * 128;             // one K-block of a KV tile
+  static constexpr int kKvStage = C::kNkb * kKvKb;
   static constexpr int kQ = 0;
-  static constexpr int kKv = kQ + C::kQsmKb * 16384;
-  static constexpr int kKvStage = C::kNkb * 8192;
-  static constexpr int kP = kKv + C::kStages * kKvStage;
-  static constexpr int kLive = kP + 16384;
-  static constexpr int kTotal = kLive + C::kStages * kTileKeys + 1024;
+  static constexpr int kKv = kQ + kQsmKb * 16384;
+  static constexpr int kP = kKv + kStages * kKvStage;
+  static constexpr int kRow = kP + 16384;
+  static constexpr int kLive = kRow + kMaxSlots * 4;
+  static constexpr int kCoord = kLive + kStages * kTileKeys;
+  static constexpr int kTotal = kCoord + kStages * kTileKeys * 4 + 1024;
+  static_assert((C::kDkTmem / 64) * 16384 <= kStages * kKvStage, "q staging does not fit");
 };
 
 struct MlaParams {
-  const uint16_t* q;   // bf16 [T, H, DK]
-  const uint16_t* kv;  // bf16 paged
-  int64_t kv_block_stride;
-  int32_t num_blocks;
+  int32_t num_blocks, rows_per_block, total_rows;
   const int32_t* block_table;
   int32_t bt_stride;
   const int32_t* seq_lens;
@@ -73,10 +78,10 @@ struct MlaParams {
   const int32_t* topk;
   int32_t B, T, H, K, block_size, splits, per_split;
   float scale_log2;
-  uint16_t* out;     // bf16 [T, H, DV]
-  float* lse;        // [T, H] or null
-  float* o_part;     // [T, H, S, DV]
-  float2* ml_part;   // [T, H, S] (max in log2 units, sum)
+  uint16_t* out;    // bf16 [T, H, DV]
+  float* lse;       // [T, H] or null
+  float* o_part;    // [T, H, S, DV]
+  float2* ml_part;  // [T, H, S] (max in log2 units, sum)
   int32_t* dev_status;
 };
 
@@ -95,16 +100,21 @@ __device__ __forceinline__ int find_request(const int32_t* qsl, int B, int t) {
 }
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaParams p) {
+__global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_constant__ MlaParams p,
+                                                                 const __grid_constant__ CUtensorMap qmap,
+                                                                 const __grid_constant__ CUtensorMap kvmap) {
   using C = MlaCfg<DK, DV>;
   using L = MlaSmem<DK, DV>;
-  constexpr int kChunksRow = DK * 2 / 16;       // 16-byte chunks per KV row
-  constexpr uint32_t kColS = 0, kColO = 64, kColQ = 64 + C::kDvc;
+  constexpr uint32_t kColS = 0, kColO = kTileKeys, kColQ = kTileKeys + C::kDvc;
+  constexpr int kTmemKb = C::kDkTmem / 64;  // q K-blocks held in tensor memory
+  constexpr uint32_t kTileBytes = kTileKeys * C::kNkb * 128;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_s, bar_o;
+  __shared__ uint64_t kv_full[kStages], kv_empty[kStages], p_full[2], o_done[2], s_full, s_free, q_full;
   __shared__ uint32_t tmem_holder;
+  __shared__ int s_last_live;
+  __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = blockIdx.x % C::kDvSplit;
@@ -120,282 +130,345 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaParams
   }
   const int valid = static_cast<int>(valid64);
   const int slot0 = j * p.per_split;
-  const int slot1 = min(p.K, slot0 + p.per_split);
-  const int n_tiles = slot1 > slot0 ? (slot1 - slot0 + kTileKeys - 1) / kTileKeys : 0;
+  const int n_slots = max(0, min(p.K, slot0 + p.per_split) - slot0);
 
   uint8_t* q_sm = smem + L::kQ;
   uint8_t* kv_sm = smem + L::kKv;
   uint8_t* p_sm = smem + L::kP;
+  int* row_sm = reinterpret_cast<int*>(smem + L::kRow);
   uint8_t* live_sm = smem + L::kLive;
+  int* coord_sm = reinterpret_cast<int*>(smem + L::kCoord);
 
-  // ---- set-up: zero the KV stages when rows are narrower than the K-blocks
-  if constexpr (DK % 64 != 0) {
-    for (int i = tid; i < C::kStages * L::kKvStage / 16; i += kThreads)
-      reinterpret_cast<uint4*>(kv_sm)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&p_full[s], 4);
+      mbar_init(&o_done[s], 1);
+    }
+    mbar_init(&s_full, 1);
+    mbar_init(&s_free, 4);
+    mbar_init(&q_full, 1);
+    fence_mbar_init();
+    s_last_live = -1;
+    s_abort = 0;
   }
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&tmem_holder, C::kTmemCols);
     tmem_relinquish();
-  }
-  if (tid == 0) {
-    mbar_init(&bar_s, 1);
-    mbar_init(&bar_o, 1);
-    fence_mbar_init();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_holder;
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
 
-  // ---- q: dims [0, kDkTmem) into tensor memory, the rest into shared memory
-  {
-    const int h = tid;
-    const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(t) * p.H + h) * DK);
-#pragma unroll 1
-    for (int c = 0; c < C::kDkTmem / 32; ++c) {
-      uint32_t v[16];
-      if (h < p.H) {
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const uint4 u = __ldg(src + c * 4 + x);
-          v[4 * x] = u.x; v[4 * x + 1] = u.y; v[4 * x + 2] = u.z; v[4 * x + 3] = u.w;
-        }
-      } else {
-#pragma unroll
-        for (int x = 0; x < 16; ++x) v[x] = 0u;
-      }
-      tmem_st16(lane_base + kColQ + c * 16, v);
-    }
-    tmem_st_wait();
-    constexpr int kQChunks = C::kQsmKb * 8;
-    for (int i = tid; i < 128 * kQChunks; i += kThreads) {
-      const int row = i / kQChunks, c = i % kQChunks;
-      const int dim = C::kDkTmem + c * 8;
-      const bool ok = row < p.H && dim < DK;
-      const uint16_t* g = ok ? p.q + (static_cast<int64_t>(t) * p.H + row) * DK + dim : p.q;
-      cp_async_16(smem_u32(q_sm + (c / 8) * 16384 + sw128_offset(row, c % 8)), g, ok ? 16u : 0u);
-    }
-  }
-
-  const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-  const int32_t* idx_row = p.topk + static_cast<int64_t>(t) * p.K;
-
-  // Gathers the rows of tile `i` into stage `st`; records which slots are live.
-  auto load_tile = [&](int i, int st) {
-    uint8_t* dst = kv_sm + st * L::kKvStage;
-    const uint16_t* row_ptr = p.kv;
-    bool live = false;
-    if (lane < 16) {
-      const int kr = warp + 4 * lane;
-      const int slot = slot0 + i * kTileKeys + kr;
-      if (slot < slot1) {
-        const int idx = __ldg(idx_row + slot);
-        if (idx >= 0 && idx < valid) {
-          const int blk = __ldg(bt_row + idx / p.block_size);
-          if (blk >= 0 && blk < p.num_blocks) {
-            live = true;
-            row_ptr = p.kv + static_cast<int64_t>(blk) * p.kv_block_stride + static_cast<int64_t>(idx % p.block_size) * DK;
-          } else {
-            report(p.dev_status, DSA_DEVERR_BLOCK_OOB);
-          }
-        } else if (idx != -1) {
-          report(p.dev_status, DSA_DEVERR_INDEX_OOB);
-        }
-      }
-      live_sm[st * kTileKeys + kr] = live ? 1 : 0;
-    }
-#pragma unroll 1
-    for (int m = 0; m < 16; ++m) {
-      const int kr = warp + 4 * m;
-      const uint16_t* rp = reinterpret_cast<const uint16_t*>(
-          __shfl_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(row_ptr), m));
-      const bool lv = __shfl_sync(0xFFFFFFFFu, live, m);
-#pragma unroll
-      for (int c0 = 0; c0 < kChunksRow; c0 += 32) {
-        const int c = c0 + lane;
-        if (c < kChunksRow)
-          cp_async_16(smem_u32(dst + (c / 8) * 8192 + sw128_offset(kr, c % 8)), lv ? rp + c * 8 : p.kv, lv ? 16u : 0u);
-      }
-    }
+  auto abort_now = [&](void) {
+    s_abort = 1;
+    report(p.dev_status, DSA_DEVERR_TIMEOUT);
   };
 
-  const uint32_t idesc_qk = idesc_bf16(128, kTileKeys, false, false);
-  const uint32_t idesc_pv = idesc_bf16(128, C::kDvc, false, true);
-
-  float m_ref = kNegSentinel, l_sum = 0.f;
-  bool o_valid = false, pv_pending = false, aborted = false;
-  uint32_t s_phase = 0, o_phase = 0;
-
-  if (n_tiles > 0) load_tile(0, 0);
-  cp_async_commit();
-
-  for (int i = 0; i < n_tiles; ++i) {
-    const int st = i % C::kStages;
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t* lw = reinterpret_cast<const uint32_t*>(live_sm + st * kTileKeys);
-    uint32_t any = 0;
+  // ---- prologue: q by TMA (K-blocks [0, kTmemKb) staged in the KV area,
+  // the rest straight to q_sm); the softmax warps resolve the split's slots
+  if (tid == 128) {  // first producer thread
+    prefetch_tmap(&qmap);
+    prefetch_tmap(&kvmap);
+    mbar_arrive_expect_tx(&q_full, C::kNkb * 16384);
+    for (int kb = 0; kb < C::kNkb; ++kb) {
+      uint8_t* dst = kb < kTmemKb ? kv_sm + kb * 16384 : q_sm + (kb - kTmemKb) * 16384;
+      tma_load_3d(smem_u32(dst), &qmap, &q_full, kb * 64, 0, t);
+    }
+  }
+  if (warp < 4) {
+    const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+    const int32_t* idx_row = p.topk + static_cast<int64_t>(t) * p.K + slot0;
+    int last = -1;
+    for (int base = 0; base < n_slots; base += 128 * 8) {
+      int idx[8], blk[8];
 #pragma unroll
-    for (int x = 0; x < kTileKeys / 4; ++x) any |= lw[x];
-    const uint8_t* kv_st = kv_sm + st * L::kKvStage;
-
-    if (any && tid == 0) {  // S = Q K^T
-      const uint32_t kv0 = smem_u32(kv_st), qs0 = smem_u32(q_sm);
+      for (int u = 0; u < 8; ++u) {
+        const int sl = base + u * 128 + tid;
+        idx[u] = sl < n_slots ? __ldg(idx_row + sl) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        blk[u] = (idx[u] >= 0 && idx[u] < valid) ? __ldg(bt_row + idx[u] / p.block_size) : -1;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int sl = base + u * 128 + tid;
+        if (sl >= n_slots) continue;
+        int row = -1;
+        if (idx[u] >= 0 && idx[u] < valid) {
+          if (blk[u] >= 0 && blk[u] < p.num_blocks)
+            row = blk[u] * p.rows_per_block + idx[u] % p.block_size;
+          else
+            report(p.dev_status, DSA_DEVERR_BLOCK_OOB);
+        } else if (idx[u] != -1) {
+          report(p.dev_status, DSA_DEVERR_INDEX_OOB);
+        }
+        row_sm[sl] = row;
+        if (row >= 0) last = sl;
+      }
+    }
+    if (last >= 0) atomicMax(&s_last_live, last);
+    // q dims [0, kDkTmem) -> tensor memory (A operand of the first QK steps)
+    if (!mbar_wait(&q_full, 0)) {
+      if (lane == 0) abort_now();
+    } else {
+      const uint32_t lane_q = tmem + (static_cast<uint32_t>(warp * 32) << 16) + kColQ;
 #pragma unroll 1
-      for (int ks = 0; ks < C::kDkTmem / 16; ++ks)
-        mma_bf16_ts(tmem + kColS, tmem + kColQ + ks * 8,
-                    smem_desc(kv0 + (ks / 4) * 8192 + (ks % 4) * 32, 16, 1024, kSwizzle128B), idesc_qk, ks > 0 ? 1u : 0u);
+      for (int kb = 0; kb < kTmemKb; ++kb) {
+        uint32_t v[16];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 u = *reinterpret_cast<const uint4*>(kv_sm + kb * 16384 + sw128_offset(tid, half * 4 + c));
+            v[4 * c] = u.x;
+            v[4 * c + 1] = u.y;
+            v[4 * c + 2] = u.z;
+            v[4 * c + 3] = u.w;
+          }
+          tmem_st16(lane_q + kb * 32 + half * 16, v);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();  // the staging area is refilled by TMA next
+    }
+  }
+  tc_fence_before();
+  __syncthreads();  // q in place, slots resolved, staging area free
+  tc_fence_after();
+  const int n_tiles = s_abort ? 0 : (s_last_live + kTileKeys) / kTileKeys;
+
+  if (warp >= 4 && warp < 8) {
+    // ---------------- producer: 4 warps, 8 keys each; gathers of 4 rows by TMA
+    const int pw = warp - 4;
+    for (int i = 0; i < n_tiles && !s_abort; ++i) {
+      const int st = i % kStages;
+      if (i >= kStages && !mbar_wait(&kv_empty[st], ((i / kStages) - 1) & 1)) {
+        if (lane == 0) abort_now();
+        break;
+      }
+      if (lane < 8) {
+        const int kr = pw * 8 + lane;
+        const int sl = i * kTileKeys + kr;
+        const int row = sl < n_slots ? row_sm[sl] : -1;
+        live_sm[st * kTileKeys + kr] = row >= 0 ? 1 : 0;
+        coord_sm[st * kTileKeys + kr] = row >= 0 ? row : p.total_rows;  // out of range: zero fill
+      }
+      __syncwarp();
+      if (pw == 0 && lane == 0) mbar_arrive_expect_tx(&kv_full[st], kTileBytes);
+      if (lane < 2 * C::kNkb) {
+        const int g = 2 * pw + (lane & 1), kb = lane >> 1;
+        const int* cs = coord_sm + st * kTileKeys + 4 * g;
+        tma_gather4(smem_u32(kv_sm + st * L::kKvStage + kb * L::kKvKb + g * 512), &kvmap, &kv_full[st], kb * 64,
+                    cs[0], cs[1], cs[2], cs[3]);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issuer
+    const uint32_t idesc_qk = idesc_bf16(128, kTileKeys, false, false);
+    const uint32_t idesc_pv = idesc_bf16(128, C::kDvc, false, true);
+    const uint32_t q0s = smem_u32(q_sm), p0s = smem_u32(p_sm);
+    if (!mbar_wait(&q_full, 0) && lane == 0) abort_now();  // q_sm written by TMA
+    auto issue_pv = [&](int i) {
+      const int st = i % kStages;
+      const uint32_t v0 = smem_u32(kv_sm + st * L::kKvStage) + (r * C::kDvc / 64) * L::kKvKb;
+#pragma unroll
+      for (int ks = 0; ks < kTileKeys / 16; ++ks)
+        mma_bf16_ss(tmem + kColO, smem_desc(p0s + (i & 1) * 64 + ks * 32, 16, 1024, kSwizzle128B),
+                    smem_desc(v0 + ks * 2048, L::kKvKb, 1024, kSwizzle128B), idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+      mma_commit(&kv_empty[st]);
+      mma_commit(&o_done[i & 1]);
+    };
+    for (int i = 0; i < n_tiles && !s_abort; ++i) {
+      const int st = i % kStages;
+      bool ok = mbar_wait(&kv_full[st], (i / kStages) & 1);
+      if (ok && i >= 1) ok = mbar_wait(&s_free, (i - 1) & 1);
+      if (!ok) {
+        if (lane == 0) abort_now();
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) {  // S = Q K^T
+        const uint32_t kv0 = smem_u32(kv_sm + st * L::kKvStage);
 #pragma unroll 1
-      for (int kk = 0; kk < (DK - C::kDkTmem) / 16; ++kk)
-        mma_bf16_ss(tmem + kColS, smem_desc(qs0 + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024, kSwizzle128B),
-                    smem_desc(kv0 + (C::kDkTmem / 64 + kk / 4) * 8192 + (kk % 4) * 32, 16, 1024, kSwizzle128B),
-                    idesc_qk, 1u);
-      mma_commit(&bar_s);
+        for (int ks = 0; ks < C::kDkTmem / 16; ++ks)
+          mma_bf16_ts(tmem + kColS, tmem + kColQ + ks * 8,
+                      smem_desc(kv0 + (ks / 4) * L::kKvKb + (ks % 4) * 32, 16, 1024, kSwizzle128B), idesc_qk,
+                      ks > 0 ? 1u : 0u);
+#pragma unroll 1
+        for (int kk = 0; kk < (DK - C::kDkTmem + 15) / 16; ++kk)
+          mma_bf16_ss(tmem + kColS, smem_desc(q0s + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024, kSwizzle128B),
+                      smem_desc(kv0 + (kTmemKb + kk / 4) * L::kKvKb + (kk % 4) * 32, 16, 1024, kSwizzle128B),
+                      idesc_qk, 1u);
+        mma_commit(&s_full);
+      }
+      __syncwarp();
+      if (i >= 1) {  // O += P V for the previous tile
+        if (!mbar_wait(&p_full[(i - 1) & 1], ((i - 1) >> 1) & 1)) {
+          if (lane == 0) abort_now();
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) issue_pv(i - 1);
+        __syncwarp();
+      }
     }
-    // the previous PV must be done before its stage is refilled
-    if (pv_pending) {
-      const bool ok = mbar_wait(&bar_o, o_phase & 1);
-      ++o_phase;
-      pv_pending = false;
-      if (__syncthreads_or(!ok)) { aborted = true; break; }
+    if (n_tiles > 0 && !s_abort) {
+      const int i = n_tiles - 1;
+      if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1)) {
+        if (lane == 0) abort_now();
+      } else {
+        tc_fence_after();
+        if (lane == 0) issue_pv(i);
+        __syncwarp();
+      }
     }
-    if (i + 1 < n_tiles) load_tile(i + 1, (i + 1) % C::kStages);
-    cp_async_commit();
-    if (!any) continue;
+  } else {
+    // ---------------- softmax (thread = head row h = TMEM lane)
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float m_ref = kNegSentinel, l_sum = 0.f;
+    for (int i = 0; i < n_tiles && !s_abort; ++i) {
+      const int st = i % kStages;
+      if (!mbar_wait(&s_full, i & 1)) {
+        if (lane == 0) abort_now();
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[32];
+      tmem_ld32_sync(lane_base + kColS, sv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free);
+      if (!mbar_wait(&kv_full[st], (i / kStages) & 1)) {  // live flags of this tile
+        if (lane == 0) abort_now();
+        break;
+      }
+      const uint32_t* lw = reinterpret_cast<const uint32_t*>(live_sm + st * kTileKeys);
+      uint32_t live_bits = 0;
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const uint32_t w4 = lw[x];
+#pragma unroll
+        for (int y = 0; y < 4; ++y) live_bits |= ((w4 >> (8 * y)) & 1u) << (4 * x + y);
+      }
+      float mt = kNegSentinel;
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        const float s = ((live_bits >> x) & 1u) ? __uint_as_float(sv[x]) * p.scale_log2 : kNegSentinel;
+        sv[x] = __float_as_uint(s);
+        mt = fmaxf(mt, s);
+      }
+      float alpha = 1.f;
+      const bool rescale = mt > m_ref + kRescaleThreshold;
+      if (rescale) {
+        alpha = exp2f(m_ref - mt);
+        m_ref = mt;
+        l_sum *= alpha;
+      }
+      uint32_t pw[16];
+      float psum = 0.f;
+#pragma unroll
+      for (int x = 0; x < 16; ++x) {
+        const float a = ((live_bits >> (2 * x)) & 1u) ? exp2f(__uint_as_float(sv[2 * x]) - m_ref) : 0.f;
+        const float c = ((live_bits >> (2 * x + 1)) & 1u) ? exp2f(__uint_as_float(sv[2 * x + 1]) - m_ref) : 0.f;
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(a, c);
+        // the normaliser sums the bf16 weights that the PV product uses
+        psum += __bfloat162float(pb.x) + __bfloat162float(pb.y);
+        pw[x] = *reinterpret_cast<const uint32_t*>(&pb);
+      }
+      l_sum += psum;
+      // this half of the P buffer was last read by PV(i-2)
+      if (i >= 2 && !mbar_wait(&o_done[i & 1], ((i - 2) >> 1) & 1)) {
+        if (lane == 0) abort_now();
+        break;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(p_sm + sw128_offset(tid, (i & 1) * 4 + c)) =
+            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+      if (i >= 1 && __any_sync(0xFFFFFFFFu, rescale)) {
+        // O holds PV(0..i-1): wait for the last of them, then scale the rows
+        if (!mbar_wait(&o_done[(i - 1) & 1], ((i - 1) >> 1) & 1)) {
+          if (lane == 0) abort_now();
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < C::kDvc; c += 32) {
+          uint32_t o[32];
+          tmem_ld32_sync(lane_base + kColO + c, o);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+          tmem_st32(lane_base + kColO + c, o);
+        }
+        tmem_st_wait();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[i & 1]);
+    }
 
-    {
-      const bool ok = mbar_wait(&bar_s, s_phase & 1);
-      ++s_phase;
-      if (__syncthreads_or(!ok)) { aborted = true; break; }
+    // ---- epilogue
+    bool o_valid = n_tiles > 0 && !s_abort;
+    if (o_valid) {
+      const int i = n_tiles - 1;
+      if (!mbar_wait(&o_done[i & 1], (i >> 1) & 1)) {
+        if (lane == 0) abort_now();
+        o_valid = false;
+      }
     }
+    o_valid = __all_sync(0xFFFFFFFFu, o_valid) && !s_abort;
     tc_fence_after();
-
-    // ---- softmax over this tile (thread = head row)
-    uint32_t sv[64];
-    {
-      uint32_t a[32], c[32];
-      tmem_ld32_sync(lane_base + kColS, a);
-      tmem_ld32_sync(lane_base + kColS + 32, c);
-#pragma unroll
-      for (int x = 0; x < 32; ++x) { sv[x] = a[x]; sv[32 + x] = c[x]; }
-    }
-    const uint8_t* live_t = live_sm + st * kTileKeys;
-    float mt = kNegSentinel;
-#pragma unroll
-    for (int x = 0; x < 64; ++x) {
-      const float s = live_t[x] ? __uint_as_float(sv[x]) * p.scale_log2 : kNegSentinel;
-      sv[x] = __float_as_uint(s);
-      mt = fmaxf(mt, s);
-    }
-    float alpha = 1.f;
-    const bool rescale = mt > m_ref + kRescaleThreshold;
-    if (rescale) {
-      alpha = exp2f(m_ref - mt);
-      m_ref = mt;
-      l_sum *= alpha;
-    }
-    uint32_t pw[32];
-    float psum = 0.f;
-#pragma unroll
-    for (int x = 0; x < 32; ++x) {
-      const float p0 = live_t[2 * x] ? exp2f(__uint_as_float(sv[2 * x]) - m_ref) : 0.f;
-      const float p1 = live_t[2 * x + 1] ? exp2f(__uint_as_float(sv[2 * x + 1]) - m_ref) : 0.f;
-      const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-      // the normaliser adds the bf16 weights that the PV product uses
-      psum += __bfloat162float(pb.x) + __bfloat162float(pb.y);
-      pw[x] = *reinterpret_cast<const uint32_t*>(&pb);
-    }
-    l_sum += psum;
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<uint4*>(p_sm + sw128_offset(tid, c)) = make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-    if (o_valid && __any_sync(0xFFFFFFFFu, rescale)) {
+    const int h = tid;
+    const bool have = o_valid && l_sum > 0.f;
+    if (p.splits == 1) {
+      const float inv = have ? 1.f / l_sum : 0.f;
+      uint16_t* dst = p.out + (static_cast<int64_t>(t) * p.H + h) * DV + r * C::kDvc;
 #pragma unroll 1
       for (int c = 0; c < C::kDvc; c += 32) {
         uint32_t o[32];
-        tmem_ld32_sync(lane_base + kColO + c, o);
+        if (o_valid) tmem_ld32_sync(lane_base + kColO + c, o);
+        if (h < p.H) {
+          uint32_t w[16];
 #pragma unroll
-        for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-        tmem_st32(lane_base + kColO + c, o);
+          for (int x = 0; x < 16; ++x)
+            w[x] = have ? pack_bf16(__uint_as_float(o[2 * x]) * inv, __uint_as_float(o[2 * x + 1]) * inv) : 0u;
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) d4[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+        }
       }
-      tmem_st_wait();
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {  // O += P V
-      const uint32_t p0 = smem_u32(p_sm), v0 = smem_u32(kv_st) + (r * C::kDvc / 64) * 8192;
-#pragma unroll
-      for (int ks = 0; ks < kTileKeys / 16; ++ks)
-        mma_bf16_ss(tmem + kColO, smem_desc(p0 + ks * 32, 16, 1024, kSwizzle128B),
-                    smem_desc(v0 + ks * 2048, 8192, 1024, kSwizzle128B), idesc_pv, (o_valid || ks > 0) ? 1u : 0u);
-      mma_commit(&bar_o);
-    }
-    o_valid = true;
-    pv_pending = true;
-  }
-  cp_async_wait<0>();
-  if (pv_pending && !aborted) {
-    const bool ok = mbar_wait(&bar_o, o_phase & 1);
-    if (__syncthreads_or(!ok)) aborted = true;
-  }
-  tc_fence_after();
-  if (aborted) {
-    if (tid == 0) report(p.dev_status, DSA_DEVERR_TIMEOUT);
-    o_valid = false;
-    l_sum = 0.f;
-  }
-
-  // ---- epilogue
-  const int h = tid;
-  const bool have = o_valid && l_sum > 0.f;
-  if (p.splits == 1) {
-    const float inv = have ? 1.f / l_sum : 0.f;
-    uint16_t* dst = p.out + (static_cast<int64_t>(t) * p.H + h) * DV + r * C::kDvc;
+      if (r == 0 && h < p.H && p.lse != nullptr)
+        p.lse[static_cast<int64_t>(t) * p.H + h] = have ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
+    } else {
+      const int64_t row = (static_cast<int64_t>(t) * p.H + h) * p.splits + j;
+      float* dst = p.o_part + row * DV + r * C::kDvc;
 #pragma unroll 1
-    for (int c = 0; c < C::kDvc; c += 32) {
-      uint32_t o[32];
-      if (o_valid) tmem_ld32_sync(lane_base + kColO + c, o);
-      if (h < p.H) {
-        uint32_t w[16];
+      for (int c = 0; c < C::kDvc; c += 32) {
+        uint32_t o[32];
+        if (o_valid) tmem_ld32_sync(lane_base + kColO + c, o);
+        if (h < p.H) {
+          float4* d4 = reinterpret_cast<float4*>(dst + c);
 #pragma unroll
-        for (int x = 0; x < 16; ++x)
-          w[x] = have ? pack_bf16(__uint_as_float(o[2 * x]) * inv, __uint_as_float(o[2 * x + 1]) * inv) : 0u;
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-#pragma unroll
-        for (int x = 0; x < 4; ++x) d4[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+          for (int x = 0; x < 8; ++x)
+            d4[x] = o_valid ? make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
+                                          __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3]))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
+      if (r == 0 && h < p.H) p.ml_part[row] = make_float2(o_valid ? m_ref : kNegSentinel, o_valid ? l_sum : 0.f);
     }
-    if (r == 0 && h < p.H && p.lse != nullptr)
-      p.lse[static_cast<int64_t>(t) * p.H + h] = have ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
-  } else {
-    const int64_t row = (static_cast<int64_t>(t) * p.H + h) * p.splits + j;
-    float* dst = p.o_part + row * DV + r * C::kDvc;
-#pragma unroll 1
-    for (int c = 0; c < C::kDvc; c += 32) {
-      uint32_t o[32];
-      if (o_valid) tmem_ld32_sync(lane_base + kColO + c, o);
-      if (h < p.H) {
-        float4* d4 = reinterpret_cast<float4*>(dst + c);
-#pragma unroll
-        for (int x = 0; x < 8; ++x)
-          d4[x] = o_valid ? make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
-                                        __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3]))
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    if (r == 0 && h < p.H) p.ml_part[row] = make_float2(o_valid ? m_ref : kNegSentinel, o_valid ? l_sum : 0.f);
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, C::kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 // a4: out = sum_j 2^(m_j-M) o_j / sum_j 2^(m_j-M) l_j, M = max_j m_j (log2 units).
@@ -431,18 +504,38 @@ bool g_smem_big = false, g_smem_tiny = false;
 
 int dv_split_for(int Dv) { return Dv == 512 ? 2 : 1; }
 
-dsa_status_t launch_mla(const MlaParams& p, int Dk, int Dv, cudaStream_t s) {
+// q [T, H, Dk] as a 3-D tensor (box: 64 dims x 128 heads x 1 token) and the
+// latent cache as 2-D rows of Dk (box: 64 dims x 1 row, gathered 4 rows at a
+// time); both 128-byte swizzled to match the MMA operand layout.
+dsa_status_t launch_mla(const MlaParams& p, const void* q, const void* kv, int Dk, int Dv, cudaStream_t s) {
   const int64_t grid = static_cast<int64_t>(p.T) * p.splits * dv_split_for(Dv);
   if (grid > 0x7FFFFFFF) return fail(DSA_ERR_UNSUPPORTED, "sparse_mla: grid too large");
+  CUtensorMap qmap, kvmap;
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(Dk), static_cast<uint64_t>(p.H), static_cast<uint64_t>(p.T)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(Dk) * 2, static_cast<uint64_t>(p.H) * Dk * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    dsa_status_t st = make_tmap(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != DSA_OK) return st;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(Dk), static_cast<uint64_t>(std::max(p.total_rows, 1))};
+    const uint64_t strides[1] = {static_cast<uint64_t>(Dk) * 2};
+    const uint32_t box[2] = {64, 1};
+    dsa_status_t st = make_tmap(&kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv, dims, strides, box,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != DSA_OK) return st;
+  }
   dsa_status_t st;
   if (Dk == 576) {
     st = allow_smem(sparse_mla_kernel<576, 512>, MlaSmem<576, 512>::kTotal, g_smem_big);
     if (st != DSA_OK) return st;
-    sparse_mla_kernel<576, 512><<<static_cast<unsigned>(grid), kThreads, MlaSmem<576, 512>::kTotal, s>>>(p);
+    sparse_mla_kernel<576, 512><<<static_cast<unsigned>(grid), kThreads, MlaSmem<576, 512>::kTotal, s>>>(p, qmap, kvmap);
   } else {
     st = allow_smem(sparse_mla_kernel<80, 64>, MlaSmem<80, 64>::kTotal, g_smem_tiny);
     if (st != DSA_OK) return st;
-    sparse_mla_kernel<80, 64><<<static_cast<unsigned>(grid), kThreads, MlaSmem<80, 64>::kTotal, s>>>(p);
+    sparse_mla_kernel<80, 64><<<static_cast<unsigned>(grid), kThreads, MlaSmem<80, 64>::kTotal, s>>>(p, qmap, kvmap);
   }
   return check_launch("sparse_mla_kernel");
 }
@@ -465,22 +558,25 @@ dsa_status_t validate(const void* q, const void* kv_cache, int64_t kv_block_stri
     return fail(DSA_ERR_INVALID_ARG, "%s: null pointer", name);
   if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out))
     return fail(DSA_ERR_INVALID_ARG, "%s: q, kv_cache and out must be 16-byte aligned", name);
-  if (kv_block_stride < static_cast<int64_t>(block_size) * Dk || kv_block_stride % 8)
-    return fail(DSA_ERR_INVALID_ARG, "%s: kv_block_stride %lld must be >= block_size*Dk and a multiple of 8", name,
+  if (kv_block_stride < static_cast<int64_t>(block_size) * Dk)
+    return fail(DSA_ERR_INVALID_ARG, "%s: kv_block_stride %lld < block_size*Dk", name,
                 static_cast<long long>(kv_block_stride));
+  if (kv_block_stride % Dk)
+    return fail(DSA_ERR_UNSUPPORTED, "%s: kv_block_stride %lld is not a whole number of %d-element rows", name,
+                static_cast<long long>(kv_block_stride), Dk);
+  if (static_cast<int64_t>(num_blocks) * (kv_block_stride / Dk) >= (int64_t(1) << 31))
+    return fail(DSA_ERR_UNSUPPORTED, "%s: the cache holds 2^31 rows or more", name);
   return check_device();
 }
 
-MlaParams make_params(const void* q, const void* kv_cache, int64_t kv_block_stride, int32_t num_blocks,
-                      const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
-                      const int32_t* query_start_loc, const int32_t* topk_idx, int32_t B, int32_t T, int32_t H,
-                      int32_t index_topk, int32_t block_size, float softmax_scale, int32_t splits, void* out,
-                      float* lse, int32_t* dev_status) {
+MlaParams make_params(int64_t kv_block_stride, int32_t Dk, int32_t num_blocks, const int32_t* block_table,
+                      int32_t bt_stride, const int32_t* seq_lens, const int32_t* query_start_loc,
+                      const int32_t* topk_idx, int32_t B, int32_t T, int32_t H, int32_t index_topk, int32_t block_size,
+                      float softmax_scale, int32_t splits, void* out, float* lse, int32_t* dev_status) {
   MlaParams p;
-  p.q = static_cast<const uint16_t*>(q);
-  p.kv = static_cast<const uint16_t*>(kv_cache);
-  p.kv_block_stride = kv_block_stride;
   p.num_blocks = num_blocks;
+  p.rows_per_block = static_cast<int32_t>(kv_block_stride / Dk);
+  p.total_rows = static_cast<int32_t>(static_cast<int64_t>(num_blocks) * p.rows_per_block);
   p.block_table = block_table;
   p.bt_stride = bt_stride;
   p.seq_lens = seq_lens;
@@ -515,7 +611,7 @@ extern "C" size_t sparse_mla_workspace_size(int32_t T, int32_t H, int32_t Dv, in
 extern "C" int32_t sparse_mla_auto_splits(int32_t T, int32_t H, int32_t Dv, int32_t index_topk) {
   (void)H;
   if (T <= 0 || index_topk <= 0) return 1;
-  const int tiles = (index_topk + kTileKeys - 1) / kTileKeys;
+  const int tiles = (index_topk + 63) / 64;  // work granule of the cost model
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) {
     int v = 0;
@@ -524,9 +620,9 @@ extern "C" int32_t sparse_mla_auto_splits(int32_t T, int32_t H, int32_t Dv, int3
     cudaGetLastError();
   }
   const int64_t units = static_cast<int64_t>(T) * dv_split_for(Dv);
-  int best = 1;
+  int best = (index_topk + kMaxSlots - 1) / kMaxSlots;
   int64_t best_cost = INT64_MAX;
-  for (int s = 1; s <= std::min(32, tiles); ++s) {
+  for (int s = (index_topk + kMaxSlots - 1) / kMaxSlots; s <= std::min(32, tiles); ++s) {
     const int64_t waves = (units * s + sms - 1) / sms;
     const int64_t cost = waves * ((tiles + s - 1) / s + 2);
     if (cost < best_cost) {
@@ -551,10 +647,12 @@ extern "C" dsa_status_t sparse_mla_decode(const void* q, const void* kv_cache, i
   if (num_kv_splits < 0 || num_kv_splits > 32)
     return fail(DSA_ERR_INVALID_ARG, "sparse_mla_decode: num_kv_splits %d not in [0, 32]", num_kv_splits);
   int splits = num_kv_splits == 0 ? sparse_mla_auto_splits(T, H, Dv, index_topk) : num_kv_splits;
+  if ((index_topk + splits - 1) / splits > kMaxSlots)
+    return fail(DSA_ERR_UNSUPPORTED, "sparse_mla_decode: %d top-k slots per split exceed %d", (index_topk + splits - 1) / splits,
+                kMaxSlots);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  MlaParams p = make_params(q, kv_cache, kv_block_stride, num_blocks, block_table, bt_stride, seq_lens,
-                            query_start_loc, topk_idx, B, T, H, index_topk, block_size, softmax_scale, splits, out,
-                            lse, dev_status);
+  MlaParams p = make_params(kv_block_stride, Dk, num_blocks, block_table, bt_stride, seq_lens, query_start_loc,
+                            topk_idx, B, T, H, index_topk, block_size, softmax_scale, splits, out, lse, dev_status);
   if (splits > 1) {
     const size_t need = sparse_mla_workspace_size(T, H, Dv, splits);
     if (workspace == nullptr || ws_bytes < need || !aligned16(workspace))
@@ -563,7 +661,7 @@ extern "C" dsa_status_t sparse_mla_decode(const void* q, const void* kv_cache, i
     p.o_part = static_cast<float*>(workspace);
     p.ml_part = reinterpret_cast<float2*>(p.o_part + static_cast<int64_t>(T) * H * splits * Dv);
   }
-  st = launch_mla(p, Dk, Dv, s);
+  st = launch_mla(p, q, kv_cache, Dk, Dv, s);
   if (st != DSA_OK || splits == 1) return st;
   mla_merge_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, s>>>(p.o_part, p.ml_part, splits, Dv,
                                                                                     p.out, lse);
@@ -580,8 +678,10 @@ extern "C" dsa_status_t sparse_mla_prefill(const void* q, const void* kv_cache, 
                              query_start_loc, topk_idx, B, T, H, Dk, Dv, index_topk, block_size, softmax_scale, out,
                              "sparse_mla_prefill");
   if (st != DSA_OK || T == 0) return st;
-  MlaParams p = make_params(q, kv_cache, kv_block_stride, num_blocks, block_table, bt_stride, seq_lens,
-                            query_start_loc, topk_idx, B, T, H, index_topk, block_size, softmax_scale, 1, out, lse,
-                            dev_status);
-  return launch_mla(p, Dk, Dv, reinterpret_cast<cudaStream_t>(stream));
+  if (index_topk > kMaxSlots)
+    return fail(DSA_ERR_UNSUPPORTED, "sparse_mla_prefill: index_topk %d > %d (use sparse_mla_decode with splits)",
+                index_topk, kMaxSlots);
+  MlaParams p = make_params(kv_block_stride, Dk, num_blocks, block_table, bt_stride, seq_lens, query_start_loc,
+                            topk_idx, B, T, H, index_topk, block_size, softmax_scale, 1, out, lse, dev_status);
+  return launch_mla(p, q, kv_cache, Dk, Dv, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -152,6 +152,31 @@ __device__ void block_select(const float* __restrict__ vals, const int32_t* __re
   const uint32_t thr = prefix;
 
   // ordered compaction: everything above thr, then the first `need` equal to thr
+  if (kcache != nullptr) {
+    // staged rows: each thread owns one contiguous segment, one block scan
+    const int seg = (n + kThreads - 1) / kThreads;
+    const int lo = min(n, tid * seg), hi = min(n, lo + seg);
+    uint32_t cg = 0, ce = 0;
+    for (int i = lo; i < hi; ++i) {
+      const uint32_t key = kcache[i];
+      cg += key > thr;
+      ce += key == thr;
+    }
+    uint32_t total;
+    const uint32_t before = block_exclusive_scan(cg | (ce << 16), total, sh);
+    uint32_t g = before & 0xFFFFu, e = before >> 16;
+    for (int i = lo; i < hi; ++i) {
+      const uint32_t key = kcache[i];
+      if (key > thr) {
+        emit(i, static_cast<int>(g + min(e, static_cast<uint32_t>(need))));
+        ++g;
+      } else if (key == thr) {
+        if (e < static_cast<uint32_t>(need)) emit(i, static_cast<int>(g + e));
+        ++e;
+      }
+    }
+    return;
+  }
   uint32_t run_gt = 0, run_eq = 0;
   for (int start = 0; start < n; start += kThreads) {
     const int i = start + tid;

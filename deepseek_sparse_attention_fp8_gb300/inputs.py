@@ -92,7 +92,7 @@ def _e4m3_codes(x: np.ndarray) -> np.ndarray:
 
 
 def make_workload(name: str, seed: int | None = None, *, B: int | None = None, L=None, q_len: int | None = None,
-                  index_topk: int | None = None, ld_pad: int = 128, lens=None) -> Workload:
+                  index_topk: int | None = None, ld_pad: int = 128, lens=None, block_size: int = 64) -> Workload:
     """Build one of the named workloads (optionally overriding a few sizes
     for smaller parity cases). `lens` gives explicit per-request lengths."""
     spec = dict(WORKLOADS[name])
@@ -107,7 +107,7 @@ def make_workload(name: str, seed: int | None = None, *, B: int | None = None, L
     rng = np.random.Generator(np.random.PCG64(spec["seed"] if seed is None else seed))
     Bn, qn = spec["B"], spec["q_len"]
     Hi, Di, H, Dk, Dv = spec["Hi"], spec["Di"], spec["H"], spec["Dk"], spec["Dv"]
-    bs = 64
+    bs = block_size
 
     if lens is not None:
         seq_lens = np.asarray(lens, dtype=np.int32)

@@ -23,6 +23,7 @@ SMALL = {
     "decode_topk_small": ("decode_b32_l8192", dict(lens=[300, 129, 64, 4000], index_topk=256)),
     "mtp2_small": ("mixed_b64_mtp2", dict(lens=[1500, 2049, 3000, 65], index_topk=2048)),
     "prefill_small": ("prefill_4096_of_65536", dict(L=2300, q_len=260, index_topk=512)),
+    "decode_bs128": ("decode_b32_l8192", dict(lens=[3000, 1111], index_topk=2048, block_size=128)),
 }
 
 
