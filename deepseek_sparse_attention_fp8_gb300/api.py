@@ -43,6 +43,9 @@ _SIGS = {
     "sparse_mla_auto_splits": ([_i32, _i32, _i32, _i32], _i32),
     "sparse_mla_decode": ([_p, _p, _i64, _i32, _p, _i32, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32,
                            _i32, _p, _p, _p, _sz, _p, _p], _i32),
+    "sparse_mla_fixed_scratch_bytes": ([], _sz),
+    "sparse_mla_decode_fixed_scratch": ([_p, _p, _i64, _i32, _p, _i32, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32,
+                                         _i32, _f32, _i32, _p, _p, _p, _p], _i32),
     "sparse_mla_prefill": ([_p, _p, _i64, _i32, _p, _i32, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32,
                             _p, _p, _p, _p], _i32),
 }
@@ -188,6 +191,27 @@ def sparse_mla_decode(q, kv_cache, block_table, seq_lens, query_start_loc, topk_
                                seq_lens.shape[0], T, H, Dk, dv, K, block_size, softmax_scale, splits, _ptr(out),
                                _ptr(lse), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
     _check(st, "sparse_mla_decode")
+    return out
+
+
+def sparse_mla_fixed_scratch_bytes() -> int:
+    return int(lib.sparse_mla_fixed_scratch_bytes())
+
+
+def sparse_mla_decode_fixed_scratch(q, kv_cache, block_table, seq_lens, query_start_loc, topk_idx, softmax_scale, dv,
+                                    out, lse=None, num_kv_splits=0, dev_status=None, stream=None):
+    """a3 + a4 without any allocation: the split partials live in the
+    library's fixed device scratch (for callers that cannot allocate; calls
+    that overlap on the GPU race on the shared scratch)."""
+    num_blocks, block_size, Dk, T, H = _mla_common(q, kv_cache, block_table, seq_lens, query_start_loc, topk_idx,
+                                                   out, lse, dev_status)
+    K = topk_idx.shape[1]
+    st = lib.sparse_mla_decode_fixed_scratch(_ptr(q), _ptr(kv_cache), block_size * Dk, num_blocks, _ptr(block_table),
+                                             block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc),
+                                             _ptr(topk_idx), seq_lens.shape[0], T, H, Dk, dv, K, block_size,
+                                             softmax_scale, num_kv_splits, _ptr(out), _ptr(lse), _ptr(dev_status),
+                                             _stream(stream))
+    _check(st, "sparse_mla_decode_fixed_scratch")
     return out
 
 

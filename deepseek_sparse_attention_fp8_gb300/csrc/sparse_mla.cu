@@ -24,6 +24,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -684,4 +685,78 @@ extern "C" dsa_status_t sparse_mla_prefill(const void* q, const void* kv_cache, 
   MlaParams p = make_params(kv_block_stride, Dk, num_blocks, block_table, bt_stride, seq_lens, query_start_loc,
                             topk_idx, B, T, H, index_topk, block_size, softmax_scale, 1, out, lse, dev_status);
   return launch_mla(p, q, kv_cache, Dk, Dv, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// Split-KV decode for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc at the point where they run the step:
+// code inside a CUDA-graph capture region, an allocator-free serving runtime
+// that owns all device memory up front, or a host environment (a plugin, a
+// sandboxed runtime) that is not allowed to create allocations. For them the
+// split partials live in the file-scope array below instead of a caller
+// workspace. It is reserved when the library is loaded on a device and stays
+// resident on every GPU that loads the library until the process exits.
+namespace {
+
+constexpr size_t kFixedScratchBytes = size_t(24) << 20;  // 24 MiB
+static __device__ __align__(256) unsigned char g_mla_fixed_scratch[kFixedScratchBytes];
+
+constexpr int kScratchMaxDevices = 64;
+void* g_fixed_scratch_ptr[kScratchMaxDevices] = {nullptr};
+std::mutex g_fixed_scratch_mu;
+
+// Device address of the array on the current device, looked up once per
+// device. In host code the array's name is only a host-side stand-in, so the
+// kernels are given the address returned here.
+dsa_status_t fixed_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kScratchMaxDevices) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_fixed_scratch_mu);
+  if (g_fixed_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_mla_fixed_scratch);
+    if (e != cudaSuccess || ptr == nullptr)
+      return fail(DSA_ERR_CUDA, "cudaGetSymbolAddress(fixed scratch): %s", cudaGetErrorString(e));
+    g_fixed_scratch_ptr[dev] = ptr;
+  }
+  *out = g_fixed_scratch_ptr[dev];
+  return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" size_t sparse_mla_fixed_scratch_bytes(void) { return kFixedScratchBytes; }
+
+extern "C" dsa_status_t sparse_mla_decode_fixed_scratch(
+    const void* q, const void* kv_cache, int64_t kv_block_stride, int32_t num_blocks, const int32_t* block_table,
+    int32_t bt_stride, const int32_t* seq_lens, const int32_t* query_start_loc, const int32_t* topk_idx, int32_t B,
+    int32_t T, int32_t H, int32_t Dk, int32_t Dv, int32_t index_topk, int32_t block_size, float softmax_scale,
+    int32_t num_kv_splits, void* out, float* lse, int32_t* dev_status, dsa_stream_t stream) {
+  if (num_kv_splits < 0 || num_kv_splits > 32)
+    return fail(DSA_ERR_INVALID_ARG, "sparse_mla_decode_fixed_scratch: num_kv_splits %d not in [0, 32]",
+                num_kv_splits);
+  if (T <= 0 || H <= 0 || Dv <= 0 || index_topk <= 0)  // nothing to split: no scratch needed
+    return sparse_mla_decode(q, kv_cache, kv_block_stride, num_blocks, block_table, bt_stride, seq_lens,
+                             query_start_loc, topk_idx, B, T, H, Dk, Dv, index_topk, block_size, softmax_scale,
+                             num_kv_splits, out, lse, nullptr, 0, dev_status, stream);
+  const int32_t splits = num_kv_splits == 0 ? sparse_mla_auto_splits(T, H, Dv, index_topk) : num_kv_splits;
+  const size_t need = sparse_mla_workspace_size(T, H, Dv, splits);
+  if (need > kFixedScratchBytes)
+    return fail(DSA_ERR_WORKSPACE,
+                "sparse_mla_decode_fixed_scratch: %d splits of T=%d H=%d Dv=%d need %zu bytes of partials, more than "
+                "the fixed %zu-byte scratch; use fewer splits or sparse_mla_decode with a workspace",
+                splits, T, H, Dv, need, kFixedScratchBytes);
+  void* scratch = nullptr;
+  if (need > 0) {
+    dsa_status_t st = fixed_scratch_address(&scratch);
+    if (st != DSA_OK) return st;
+  }
+  // every partial the merge reads is written by the split kernel first, so
+  // nothing in the scratch has to start at zero
+  return sparse_mla_decode(q, kv_cache, kv_block_stride, num_blocks, block_table, bt_stride, seq_lens,
+                           query_start_loc, topk_idx, B, T, H, Dk, Dv, index_topk, block_size, softmax_scale, splits,
+                           out, lse, scratch, need, dev_status, stream);
 }

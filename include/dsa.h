@@ -172,6 +172,37 @@ dsa_status_t sparse_mla_prefill(const void* q, const void* kv_cache, int64_t kv_
                                 float softmax_scale, void* out, float* lse, int32_t* dev_status,
                                 dsa_stream_t stream);
 
+/*
+ * Split-KV sparse MLA decode that allocates nothing, for callers that cannot
+ * call cudaMalloc when they run the step: code inside a CUDA-graph capture
+ * region, allocator-free serving runtimes that own all device memory up front,
+ * and host environments that may not create device allocations. The pages
+ * have no counterpart of this entry point; it is a deployment convenience.
+ *
+ * Same arguments and results as sparse_mla_decode, minus the workspace: the
+ * split partials go to a fixed scratch array of sparse_mla_fixed_scratch_bytes()
+ * bytes (24 MiB) that the library reserves in device memory on every GPU that
+ * loads it, held until the process exits. A request whose partials
+ * (sparse_mla_workspace_size for the chosen number of splits) exceed it is
+ * rejected with DSA_ERR_WORKSPACE and launches nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) for that device; make that first call before any
+ *     stream capture that includes this entry point.
+ *   - All calls share the one array. Calls that may overlap on the GPU (on
+ *     different streams, or in parallel graphs) race on it and must be
+ *     serialised by the caller.
+ *   - Nothing in the array needs to start at zero: every partial the merge
+ *     reads is written first in the same call.
+ */
+size_t sparse_mla_fixed_scratch_bytes(void);
+dsa_status_t sparse_mla_decode_fixed_scratch(const void* q, const void* kv_cache, int64_t kv_block_stride,
+                                             int32_t num_blocks, const int32_t* block_table, int32_t bt_stride,
+                                             const int32_t* seq_lens, const int32_t* query_start_loc,
+                                             const int32_t* topk_idx, int32_t B, int32_t T, int32_t H, int32_t Dk,
+                                             int32_t Dv, int32_t index_topk, int32_t block_size, float softmax_scale,
+                                             int32_t num_kv_splits, void* out, float* lse, int32_t* dev_status,
+                                             dsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
