@@ -34,40 +34,48 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 288;  // warps 0-3 softmax/epilogue, warps 4-7 loads, warp 8 MMA
-constexpr int kMmaWarp = 8;
-constexpr int kTileKeys = 32;
-constexpr int kStages = 4;
+constexpr int kThreads = 416;  // warps 0-7 softmax/epilogue, warps 8-11 loads, warp 12 MMA
+constexpr int kProdWarp0 = 8;
+constexpr int kMmaWarp = 12;
+constexpr int kTileKeys = 64;
+constexpr int kStages = 3;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 constexpr int kMaxSlots = 4096;           // top-k slots one CTA (one split) may cover
+constexpr int kXPitch = 64 * 4 + 16;      // bytes per row of the score-exchange buffer
 
+// kPair: the two CTAs of a cluster split the Dk dims (rank 0: K-blocks
+// [0, kNkb0), rank 1: the rest) and the value dims (rank r: values
+// [r*kDvc, (r+1)*kDvc)), and exchange partial scores through DSMEM.
 template <int DK, int DV>
 struct MlaCfg;
 template <>
 struct MlaCfg<576, 512> {
-  static constexpr int kDvSplit = 2, kDvc = 256, kDkTmem = 448, kNkb = 9, kTmemCols = 512;
+  static constexpr bool kPair = true;
+  static constexpr int kNkb0 = 4, kNkb1 = 5, kMaxNkb = 5, kDvc = 256, kTmemCols = 512;
 };
 template <>
 struct MlaCfg<80, 64> {
-  static constexpr int kDvSplit = 1, kDvc = 64, kDkTmem = 64, kNkb = 2, kTmemCols = 128;
+  static constexpr bool kPair = false;
+  static constexpr int kNkb0 = 2, kNkb1 = 0, kMaxNkb = 2, kDvc = 64, kTmemCols = 256;
 };
 
 template <int DK, int DV>
 struct MlaSmem {
   using C = MlaCfg<DK, DV>;
-  static constexpr int kQsmKb = C::kNkb - C::kDkTmem / 64;  // q K-blocks read from shared memory
-  static constexpr int kKvKb = kTileKeys * 128;             // one K-block of a KV tile
-  static constexpr int kKvStage = C::kNkb * kKvKb;
-  static constexpr int kQ = 0;
-  static constexpr int kKv = kQ + kQsmKb * 16384;
+  static constexpr int kKvKb = kTileKeys * 128;  // one 64-dim K-block of a KV tile
+  static constexpr int kKvStage = C::kMaxNkb * kKvKb;
+  static constexpr int kKv = 0;
   static constexpr int kP = kKv + kStages * kKvStage;
-  static constexpr int kRow = kP + 16384;
+  static constexpr int kX = kP + 16384;
+  static constexpr int kXBuf = 128 * kXPitch;
+  static constexpr int kRow = kX + (C::kPair ? 2 * kXBuf : 0);
   static constexpr int kLive = kRow + kMaxSlots * 4;
   static constexpr int kCoord = kLive + kStages * kTileKeys;
-  static constexpr int kTotal = kCoord + kStages * kTileKeys * 4 + 1024;
-  static_assert((C::kDkTmem / 64) * 16384 <= kStages * kKvStage, "q staging does not fit");
+  static constexpr int kRed = kCoord + kStages * kTileKeys * 4;
+  static constexpr int kTotal = kRed + 2 * 2 * 128 * 4 + 1024;
+  static_assert(C::kMaxNkb * 16384 <= kStages * kKvStage, "q staging does not fit");
 };
 
 struct MlaParams {
@@ -106,21 +114,23 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
                                                                  const __grid_constant__ CUtensorMap kvmap) {
   using C = MlaCfg<DK, DV>;
   using L = MlaSmem<DK, DV>;
+  constexpr int kSplitDv = C::kPair ? 2 : 1;
   constexpr uint32_t kColS = 0, kColO = kTileKeys, kColQ = kTileKeys + C::kDvc;
-  constexpr int kTmemKb = C::kDkTmem / 64;  // q K-blocks held in tensor memory
-  constexpr uint32_t kTileBytes = kTileKeys * C::kNkb * 128;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t kv_full[kStages], kv_empty[kStages], p_full[2], o_done[2], s_full, s_free, q_full;
+  __shared__ uint64_t kv_full[kStages], kv_empty[kStages], x_full[2];
+  __shared__ uint64_t s_full, s_free, p_full, o_done, q_full, pair_bar[4];
   __shared__ uint32_t tmem_holder;
   __shared__ int s_last_live;
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r = blockIdx.x % C::kDvSplit;
-  const int j = (blockIdx.x / C::kDvSplit) % p.splits;
-  const int t = blockIdx.x / (C::kDvSplit * p.splits);
+  const int r = C::kPair ? static_cast<int>(cluster_ctarank()) : 0;
+  const int j = (blockIdx.x / kSplitDv) % p.splits;
+  const int t = blockIdx.x / (kSplitDv * p.splits);
+  const int kb0 = r == 0 ? 0 : C::kNkb0;          // first K-block (64 dims) this CTA owns
+  const int nkb = r == 0 ? C::kNkb0 : C::kNkb1;   // K-blocks this CTA owns
   const int b = find_request(p.qsl, p.B, t);
   const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1);
   int64_t valid64 = static_cast<int64_t>(__ldg(p.seq_lens + b)) - (q1 - q0) + (t - q0) + 1;
@@ -133,9 +143,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   const int slot0 = j * p.per_split;
   const int n_slots = max(0, min(p.K, slot0 + p.per_split) - slot0);
 
-  uint8_t* q_sm = smem + L::kQ;
   uint8_t* kv_sm = smem + L::kKv;
   uint8_t* p_sm = smem + L::kP;
+  uint8_t* x_sm = smem + L::kX;
   int* row_sm = reinterpret_cast<int*>(smem + L::kRow);
   uint8_t* live_sm = smem + L::kLive;
   int* coord_sm = reinterpret_cast<int*>(smem + L::kCoord);
@@ -145,13 +155,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&p_full[s], 4);
-      mbar_init(&o_done[s], 1);
-    }
+    for (int s = 0; s < 2; ++s) mbar_init(&x_full[s], 1);  // local expect_tx; the peer's st.async deliver the bytes
     mbar_init(&s_full, 1);
-    mbar_init(&s_free, 4);
+    mbar_init(&s_free, 8);
+    mbar_init(&p_full, 8);
+    mbar_init(&o_done, 1);
     mbar_init(&q_full, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&pair_bar[q], 64);
     fence_mbar_init();
     s_last_live = -1;
     s_abort = 0;
@@ -161,7 +171,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (C::kPair) {
+    cluster_sync_all();  // both CTAs' barriers exist before any remote arrival
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem = tmem_holder;
 
@@ -170,26 +184,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     report(p.dev_status, DSA_DEVERR_TIMEOUT);
   };
 
-  // ---- prologue: q by TMA (K-blocks [0, kTmemKb) staged in the KV area,
-  // the rest straight to q_sm); the softmax warps resolve the split's slots
-  if (tid == 128) {  // first producer thread
+  // ---- prologue: this CTA's q K-blocks by TMA into the idle KV stage area;
+  // the softmax warps resolve the split's top-k slots to physical rows
+  if (tid == kProdWarp0 * 32) {  // first producer thread
     prefetch_tmap(&qmap);
     prefetch_tmap(&kvmap);
-    mbar_arrive_expect_tx(&q_full, C::kNkb * 16384);
-    for (int kb = 0; kb < C::kNkb; ++kb) {
-      uint8_t* dst = kb < kTmemKb ? kv_sm + kb * 16384 : q_sm + (kb - kTmemKb) * 16384;
-      tma_load_3d(smem_u32(dst), &qmap, &q_full, kb * 64, 0, t);
-    }
+    mbar_arrive_expect_tx(&q_full, nkb * 16384);
+    for (int kb = 0; kb < nkb; ++kb)
+      tma_load_3d(smem_u32(kv_sm + kb * 16384), &qmap, &q_full, (kb0 + kb) * 64, 0, t);
   }
-  if (warp < 4) {
+  if (warp < 8) {
     const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
     const int32_t* idx_row = p.topk + static_cast<int64_t>(t) * p.K + slot0;
     int last = -1;
-    for (int base = 0; base < n_slots; base += 128 * 8) {
+    for (int base = 0; base < n_slots; base += 256 * 8) {
       int idx[8], blk[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int sl = base + u * 128 + tid;
+        const int sl = base + u * 256 + tid;
         idx[u] = sl < n_slots ? __ldg(idx_row + sl) : -1;
       }
 #pragma unroll
@@ -197,15 +209,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
         blk[u] = (idx[u] >= 0 && idx[u] < valid) ? __ldg(bt_row + idx[u] / p.block_size) : -1;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int sl = base + u * 128 + tid;
+        const int sl = base + u * 256 + tid;
         if (sl >= n_slots) continue;
         int row = -1;
         if (idx[u] >= 0 && idx[u] < valid) {
           if (blk[u] >= 0 && blk[u] < p.num_blocks)
             row = blk[u] * p.rows_per_block + idx[u] % p.block_size;
-          else
+          else if (r == 0)
             report(p.dev_status, DSA_DEVERR_BLOCK_OOB);
-        } else if (idx[u] != -1) {
+        } else if (idx[u] != -1 && r == 0) {
           report(p.dev_status, DSA_DEVERR_INDEX_OOB);
         }
         row_sm[sl] = row;
@@ -213,19 +225,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       }
     }
     if (last >= 0) atomicMax(&s_last_live, last);
-    // q dims [0, kDkTmem) -> tensor memory (A operand of the first QK steps)
+    // this CTA's q dims -> tensor memory (A operand of QK)
     if (!mbar_wait(&q_full, 0)) {
       if (lane == 0) abort_now();
     } else {
-      const uint32_t lane_q = tmem + (static_cast<uint32_t>(warp * 32) << 16) + kColQ;
+      const int hq = (warp & 3) * 32 + lane;
+      const uint32_t lane_q = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kColQ;
 #pragma unroll 1
-      for (int kb = 0; kb < kTmemKb; ++kb) {
+      for (int kb = warp >> 2; kb < nkb; kb += 2) {  // the two warps of a lane group split the K-blocks
         uint32_t v[16];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const uint4 u = *reinterpret_cast<const uint4*>(kv_sm + kb * 16384 + sw128_offset(tid, half * 4 + c));
+            const uint4 u = *reinterpret_cast<const uint4*>(kv_sm + kb * 16384 + sw128_offset(hq, half * 4 + c));
             v[4 * c] = u.x;
             v[4 * c + 1] = u.y;
             v[4 * c + 2] = u.z;
@@ -243,46 +256,48 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   tc_fence_after();
   const int n_tiles = s_abort ? 0 : (s_last_live + kTileKeys) / kTileKeys;
 
-  if (warp >= 4 && warp < 8) {
-    // ---------------- producer: 4 warps, 8 keys each; gathers of 4 rows by TMA
-    const int pw = warp - 4;
+  if (warp >= kProdWarp0 && warp < kMmaWarp) {
+    // ---------------- producer: 4 warps, 16 keys each; 4-row TMA gathers of
+    // this CTA's K-blocks only
+    const int pw = warp - kProdWarp0;
+    const uint32_t tile_bytes = kTileKeys * nkb * 128;
     for (int i = 0; i < n_tiles && !s_abort; ++i) {
       const int st = i % kStages;
       if (i >= kStages && !mbar_wait(&kv_empty[st], ((i / kStages) - 1) & 1)) {
         if (lane == 0) abort_now();
         break;
       }
-      if (lane < 8) {
-        const int kr = pw * 8 + lane;
+      if (lane < 16) {
+        const int kr = pw * 16 + lane;
         const int sl = i * kTileKeys + kr;
         const int row = sl < n_slots ? row_sm[sl] : -1;
         live_sm[st * kTileKeys + kr] = row >= 0 ? 1 : 0;
         coord_sm[st * kTileKeys + kr] = row >= 0 ? row : p.total_rows;  // out of range: zero fill
       }
       __syncwarp();
-      if (pw == 0 && lane == 0) mbar_arrive_expect_tx(&kv_full[st], kTileBytes);
-      if (lane < 2 * C::kNkb) {
-        const int g = 2 * pw + (lane & 1), kb = lane >> 1;
+      if (pw == 0 && lane == 0) mbar_arrive_expect_tx(&kv_full[st], tile_bytes);
+      if (lane < 4 * nkb) {
+        const int g = pw * 4 + (lane & 3), kb = lane >> 2;
         const int* cs = coord_sm + st * kTileKeys + 4 * g;
-        tma_gather4(smem_u32(kv_sm + st * L::kKvStage + kb * L::kKvKb + g * 512), &kvmap, &kv_full[st], kb * 64,
-                    cs[0], cs[1], cs[2], cs[3]);
+        tma_gather4(smem_u32(kv_sm + st * L::kKvStage + kb * L::kKvKb + g * 512), &kvmap, &kv_full[st],
+                    (kb0 + kb) * 64, cs[0], cs[1], cs[2], cs[3]);
       }
     }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer
+    if (!mbar_wait(&q_full, 0) && lane == 0) abort_now();
     const uint32_t idesc_qk = idesc_bf16(128, kTileKeys, false, false);
     const uint32_t idesc_pv = idesc_bf16(128, C::kDvc, false, true);
-    const uint32_t q0s = smem_u32(q_sm), p0s = smem_u32(p_sm);
-    if (!mbar_wait(&q_full, 0) && lane == 0) abort_now();  // q_sm written by TMA
+    const uint32_t p0s = smem_u32(p_sm);
     auto issue_pv = [&](int i) {
       const int st = i % kStages;
-      const uint32_t v0 = smem_u32(kv_sm + st * L::kKvStage) + (r * C::kDvc / 64) * L::kKvKb;
+      const uint32_t v0 = smem_u32(kv_sm + st * L::kKvStage);  // value dims = this CTA's first K-blocks
 #pragma unroll
       for (int ks = 0; ks < kTileKeys / 16; ++ks)
-        mma_bf16_ss(tmem + kColO, smem_desc(p0s + (i & 1) * 64 + ks * 32, 16, 1024, kSwizzle128B),
+        mma_bf16_ss(tmem + kColO, smem_desc(p0s + ks * 32, 16, 1024, kSwizzle128B),
                     smem_desc(v0 + ks * 2048, L::kKvKb, 1024, kSwizzle128B), idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
       mma_commit(&kv_empty[st]);
-      mma_commit(&o_done[i & 1]);
+      mma_commit(&o_done);
     };
     for (int i = 0; i < n_tiles && !s_abort; ++i) {
       const int st = i % kStages;
@@ -293,23 +308,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
         break;
       }
       tc_fence_after();
-      if (lane == 0) {  // S = Q K^T
+      if (lane == 0) {  // this CTA's part of S = Q K^T
         const uint32_t kv0 = smem_u32(kv_sm + st * L::kKvStage);
 #pragma unroll 1
-        for (int ks = 0; ks < C::kDkTmem / 16; ++ks)
+        for (int ks = 0; ks < nkb * 4; ++ks)
           mma_bf16_ts(tmem + kColS, tmem + kColQ + ks * 8,
                       smem_desc(kv0 + (ks / 4) * L::kKvKb + (ks % 4) * 32, 16, 1024, kSwizzle128B), idesc_qk,
                       ks > 0 ? 1u : 0u);
-#pragma unroll 1
-        for (int kk = 0; kk < (DK - C::kDkTmem + 15) / 16; ++kk)
-          mma_bf16_ss(tmem + kColS, smem_desc(q0s + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024, kSwizzle128B),
-                      smem_desc(kv0 + (kTmemKb + kk / 4) * L::kKvKb + (kk % 4) * 32, 16, 1024, kSwizzle128B),
-                      idesc_qk, 1u);
         mma_commit(&s_full);
       }
       __syncwarp();
       if (i >= 1) {  // O += P V for the previous tile
-        if (!mbar_wait(&p_full[(i - 1) & 1], ((i - 1) >> 1) & 1)) {
+        if (!mbar_wait(&p_full, (i - 1) & 1)) {
           if (lane == 0) abort_now();
           break;
         }
@@ -320,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     }
     if (n_tiles > 0 && !s_abort) {
       const int i = n_tiles - 1;
-      if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1)) {
+      if (!mbar_wait(&p_full, i & 1)) {
         if (lane == 0) abort_now();
       } else {
         tc_fence_after();
@@ -329,9 +339,21 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       }
     }
   } else {
-    // ---------------- softmax (thread = head row h = TMEM lane)
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float m_ref = kNegSentinel, l_sum = 0.f;
+    // ---------------- softmax: warps w and w+4 share TMEM lanes 32*(w%4).. (one
+    // head row per thread) and take keys [32*kh, 32*kh+32) of each tile
+    const int kh = warp >> 2;            // key half
+    const int h = (warp & 3) * 32 + lane;  // head row
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    uint64_t* pbar = &pair_bar[warp & 3];  // joins the two warps of this lane group
+    float* red = reinterpret_cast<float*>(smem + L::kRed);  // [parity][key half][128 rows]
+    uint32_t x_peer = 0;
+    if constexpr (C::kPair) x_peer = mapa_shared(smem_u32(x_sm + h * kXPitch + kh * 128), static_cast<uint32_t>(r ^ 1));
+    const uint8_t* x_mine = x_sm + h * kXPitch + kh * 128;
+    uint32_t peer_x_full[2] = {0, 0};
+    if constexpr (C::kPair) {
+      for (int q = 0; q < 2; ++q) peer_x_full[q] = mapa_shared(smem_u32(&x_full[q]), static_cast<uint32_t>(r ^ 1));
+    }
+    float m_ref = kNegSentinel, l_part = 0.f;
     for (int i = 0; i < n_tiles && !s_abort; ++i) {
       const int st = i % kStages;
       if (!mbar_wait(&s_full, i & 1)) {
@@ -340,15 +362,39 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       }
       tc_fence_after();
       uint32_t sv[32];
-      tmem_ld32_sync(lane_base + kColS, sv);
+      tmem_ld32_sync(lane_base + kColS + kh * 32, sv);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free);
+      if constexpr (C::kPair) {
+        // swap partial scores with the peer CTA: S = S_rank0 + S_rank1. The
+        // peer's buffer X[i & 1] is free again: this CTA sends tile i only after
+        // receiving the peer's tile i-1, which the peer sends only after it has
+        // finished reading X[i & 1] (tile i-2).
+        const int xp = i & 1;
+        if (tid == 0) mbar_arrive_expect_tx(&x_full[xp], 128 * 64 * 4);  // the peer's whole partial tile
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_async_v4(x_peer + xp * L::kXBuf + c * 16, peer_x_full[xp], sv[4 * c], sv[4 * c + 1], sv[4 * c + 2],
+                      sv[4 * c + 3]);
+        if (!mbar_wait_cluster(&x_full[xp], (i >> 1) & 1)) {
+          if (lane == 0) abort_now();
+          break;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 u = *reinterpret_cast<const uint4*>(x_mine + xp * L::kXBuf + c * 16);
+          sv[4 * c] = __float_as_uint(__uint_as_float(sv[4 * c]) + __uint_as_float(u.x));
+          sv[4 * c + 1] = __float_as_uint(__uint_as_float(sv[4 * c + 1]) + __uint_as_float(u.y));
+          sv[4 * c + 2] = __float_as_uint(__uint_as_float(sv[4 * c + 2]) + __uint_as_float(u.z));
+          sv[4 * c + 3] = __float_as_uint(__uint_as_float(sv[4 * c + 3]) + __uint_as_float(u.w));
+        }
+      }
       if (!mbar_wait(&kv_full[st], (i / kStages) & 1)) {  // live flags of this tile
         if (lane == 0) abort_now();
         break;
       }
-      const uint32_t* lw = reinterpret_cast<const uint32_t*>(live_sm + st * kTileKeys);
+      const uint32_t* lw = reinterpret_cast<const uint32_t*>(live_sm + st * kTileKeys + kh * 32);
       uint32_t live_bits = 0;
 #pragma unroll
       for (int x = 0; x < 8; ++x) {
@@ -363,43 +409,49 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
         sv[x] = __float_as_uint(s);
         mt = fmaxf(mt, s);
       }
+      // the row maximum over both key halves (slots alternate by tile parity, so
+      // one join per tile suffices)
+      red[(i & 1) * 256 + kh * 128 + h] = mt;
+      mbar_arrive(pbar);
+      if (!mbar_wait(pbar, i & 1)) {
+        if (lane == 0) abort_now();
+        break;
+      }
+      mt = fmaxf(mt, red[(i & 1) * 256 + (kh ^ 1) * 128 + h]);
       float alpha = 1.f;
       const bool rescale = mt > m_ref + kRescaleThreshold;
       if (rescale) {
-        alpha = exp2f(m_ref - mt);
+        alpha = ex2_approx(m_ref - mt);
         m_ref = mt;
-        l_sum *= alpha;
+        l_part *= alpha;
       }
       uint32_t pw[16];
       float psum = 0.f;
 #pragma unroll
       for (int x = 0; x < 16; ++x) {
-        const float a = ((live_bits >> (2 * x)) & 1u) ? exp2f(__uint_as_float(sv[2 * x]) - m_ref) : 0.f;
-        const float c = ((live_bits >> (2 * x + 1)) & 1u) ? exp2f(__uint_as_float(sv[2 * x + 1]) - m_ref) : 0.f;
+        const float a = ((live_bits >> (2 * x)) & 1u) ? ex2_approx(__uint_as_float(sv[2 * x]) - m_ref) : 0.f;
+        const float c = ((live_bits >> (2 * x + 1)) & 1u) ? ex2_approx(__uint_as_float(sv[2 * x + 1]) - m_ref) : 0.f;
         const __nv_bfloat162 pb = __floats2bfloat162_rn(a, c);
         // the normaliser sums the bf16 weights that the PV product uses
         psum += __bfloat162float(pb.x) + __bfloat162float(pb.y);
         pw[x] = *reinterpret_cast<const uint32_t*>(&pb);
       }
-      l_sum += psum;
-      // this half of the P buffer was last read by PV(i-2)
-      if (i >= 2 && !mbar_wait(&o_done[i & 1], ((i - 2) >> 1) & 1)) {
-        if (lane == 0) abort_now();
-        break;
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(p_sm + sw128_offset(tid, (i & 1) * 4 + c)) =
-            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-      if (i >= 1 && __any_sync(0xFFFFFFFFu, rescale)) {
-        // O holds PV(0..i-1): wait for the last of them, then scale the rows
-        if (!mbar_wait(&o_done[(i - 1) & 1], ((i - 1) >> 1) & 1)) {
+      l_part += psum;
+      // P and O are free once PV of the previous tile is done
+      if (i >= 1) {
+        if (!mbar_wait(&o_done, (i - 1) & 1)) {
           if (lane == 0) abort_now();
           break;
         }
         tc_fence_after();
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(p_sm + sw128_offset(h, kh * 4 + c)) =
+            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+      if (i >= 1 && __any_sync(0xFFFFFFFFu, rescale)) {  // each warp of the pair scales half of O
 #pragma unroll 1
-        for (int c = 0; c < C::kDvc; c += 32) {
+        for (int c = kh * (C::kDvc / 2); c < (kh + 1) * (C::kDvc / 2); c += 32) {
           uint32_t o[32];
           tmem_ld32_sync(lane_base + kColO + c, o);
 #pragma unroll
@@ -411,27 +463,38 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[i & 1]);
+      if (lane == 0) mbar_arrive(&p_full);
     }
 
-    // ---- epilogue
+    // ---- epilogue: l = l_half0 + l_half1; each warp of the pair writes half of the columns
     bool o_valid = n_tiles > 0 && !s_abort;
+    float l_sum = 0.f;
+    {
+      const int e = n_tiles & 1;  // the join after the last tile
+      red[e * 256 + kh * 128 + h] = l_part;
+      mbar_arrive(pbar);
+      if (mbar_wait(pbar, n_tiles & 1)) {
+        l_sum = red[e * 256 + h] + red[e * 256 + 128 + h];
+      } else {
+        if (lane == 0) abort_now();
+        o_valid = false;
+      }
+    }
     if (o_valid) {
-      const int i = n_tiles - 1;
-      if (!mbar_wait(&o_done[i & 1], (i >> 1) & 1)) {
+      if (!mbar_wait(&o_done, (n_tiles - 1) & 1)) {
         if (lane == 0) abort_now();
         o_valid = false;
       }
     }
     o_valid = __all_sync(0xFFFFFFFFu, o_valid) && !s_abort;
     tc_fence_after();
-    const int h = tid;
     const bool have = o_valid && l_sum > 0.f;
+    constexpr int kHalf = C::kDvc / 2;
     if (p.splits == 1) {
       const float inv = have ? 1.f / l_sum : 0.f;
       uint16_t* dst = p.out + (static_cast<int64_t>(t) * p.H + h) * DV + r * C::kDvc;
 #pragma unroll 1
-      for (int c = 0; c < C::kDvc; c += 32) {
+      for (int c = kh * kHalf; c < (kh + 1) * kHalf; c += 32) {
         uint32_t o[32];
         if (o_valid) tmem_ld32_sync(lane_base + kColO + c, o);
         if (h < p.H) {
@@ -444,13 +507,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
           for (int x = 0; x < 4; ++x) d4[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
         }
       }
-      if (r == 0 && h < p.H && p.lse != nullptr)
+      if (r == 0 && kh == 0 && h < p.H && p.lse != nullptr)
         p.lse[static_cast<int64_t>(t) * p.H + h] = have ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
     } else {
       const int64_t row = (static_cast<int64_t>(t) * p.H + h) * p.splits + j;
       float* dst = p.o_part + row * DV + r * C::kDvc;
 #pragma unroll 1
-      for (int c = 0; c < C::kDvc; c += 32) {
+      for (int c = kh * kHalf; c < (kh + 1) * kHalf; c += 32) {
         uint32_t o[32];
         if (o_valid) tmem_ld32_sync(lane_base + kColO + c, o);
         if (h < p.H) {
@@ -462,12 +525,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
                             : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      if (r == 0 && h < p.H) p.ml_part[row] = make_float2(o_valid ? m_ref : kNegSentinel, o_valid ? l_sum : 0.f);
+      if (r == 0 && kh == 0 && h < p.H)
+        p.ml_part[row] = make_float2(o_valid ? m_ref : kNegSentinel, o_valid ? l_sum : 0.f);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (C::kPair) cluster_sync_all();  // no remote access may target an exited CTA
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
@@ -532,7 +597,21 @@ dsa_status_t launch_mla(const MlaParams& p, const void* q, const void* kv, int D
   if (Dk == 576) {
     st = allow_smem(sparse_mla_kernel<576, 512>, MlaSmem<576, 512>::kTotal, g_smem_big);
     if (st != DSA_OK) return st;
-    sparse_mla_kernel<576, 512><<<static_cast<unsigned>(grid), kThreads, MlaSmem<576, 512>::kTotal, s>>>(p, qmap, kvmap);
+    // the two value halves of a (token, split) form a 2-CTA cluster
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = MlaSmem<576, 512>::kTotal;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel<576, 512>, p, qmap, kvmap);
+    if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "sparse_mla_kernel launch failed: %s", cudaGetErrorString(e));
   } else {
     st = allow_smem(sparse_mla_kernel<80, 64>, MlaSmem<80, 64>::kTotal, g_smem_tiny);
     if (st != DSA_OK) return st;
