@@ -187,28 +187,45 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
       for (int i = tid; i < S * kTileBytes / 16; i += kThreads) reinterpret_cast<uint4*>(sk)[i] = make_uint4(0, 0, 0, 0);
     }
     if (warp < 4) {
-      // a0: quantise the token block's queries into the B operand (N rows x 128 B)
-      for (int base = 0; base < n_cols; base += 128 / 8) {
-        const int n = base + tid / 8, c = tid % 8;
-        const int j = n / p.hi_pad, h = n % p.hi_pad;
-        const bool row_ok = j < ntok && h < p.Hi;
-        uint4 a = make_uint4(0, 0, 0, 0), bq = a;
-        if (row_ok && c < DI / 16) {
-          const uint4* src =
-              reinterpret_cast<const uint4*>(p.q + (tok0 + j) * p.q_stride_t + static_cast<int64_t>(h) * DI) + 2 * c;
-          a = __ldg(src);
-          bq = __ldg(src + 1);
+      // a0: quantise the token block's queries into the B operand (N rows x 128 B).
+      // 16 rows per pass (8 lanes per row); the loads of up to 4 passes are
+      // issued together so their latencies overlap.
+      for (int base0 = 0; base0 < n_cols; base0 += 4 * 16) {
+        uint4 a[4], bq[4];
+        float wv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int n = base0 + u * 16 + tid / 8, c = tid % 8;
+          const int j = n / p.hi_pad, h = n % p.hi_pad;
+          a[u] = make_uint4(0, 0, 0, 0);
+          bq[u] = a[u];
+          wv[u] = 0.f;
+          if (n < n_cols && j < ntok && h < p.Hi) {
+            if (c < DI / 16) {
+              const uint4* src =
+                  reinterpret_cast<const uint4*>(p.q + (tok0 + j) * p.q_stride_t + static_cast<int64_t>(h) * DI) + 2 * c;
+              a[u] = __ldg(src);
+              bq[u] = __ldg(src + 1);
+            }
+            if (c == 0) wv[u] = __ldg(p.w + static_cast<int64_t>(tok0 + j) * p.Hi + h);
+          }
         }
-        float scale;
-        const uint4 codes = quant_chunk16(a, bq, scale);
-        *reinterpret_cast<uint4*>(sq + sw128_offset(n, c)) = codes;
-        if (c == 0) sw[n] = row_ok ? __ldg(p.w + static_cast<int64_t>(tok0 + j) * p.Hi + h) * scale : 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int n = base0 + u * 16 + tid / 8, c = tid % 8;
+          if (base0 + u * 16 >= n_cols) break;  // uniform across the block
+          float scale;
+          const uint4 codes = quant_chunk16(a[u], bq[u], scale);
+          *reinterpret_cast<uint4*>(sq + sw128_offset(n, c)) = codes;
+          if (c == 0) sw[n] = wv[u] * scale;  // zero for padded rows
+        }
       }
-    }
-    // block ids of every key this CTA reads
-    for (int i = tid; i < n_blk; i += kThreads) {
-      const int lb = blk0 + i;
-      s_blk[i] = lb * p.block_size < seq_len ? __ldg(bt_row + lb) : -1;
+    } else {
+      // block ids of every key this CTA reads (warps 4 and 5)
+      for (int i = tid - 128; i < n_blk; i += 64) {
+        const int lb = blk0 + i;
+        s_blk[i] = lb * p.block_size < seq_len ? __ldg(bt_row + lb) : -1;
+      }
     }
     fence_proxy_async_smem();
     if (warp == 5) {

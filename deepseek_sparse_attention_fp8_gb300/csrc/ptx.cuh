@@ -171,6 +171,20 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, uint
       "l"(tmap), "r"(smem_u32(bar)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
       : "memory");
 }
+// L2 prefetch of the same four rows (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_gather4(const void* tmap, int32_t col, int32_t r0, int32_t r1, int32_t r2,
+                                                     int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.2d.L2.global.tile::gather4 [%0, {%1, %2, %3, %4, %5}];" ::"l"(tmap), "r"(col),
+      "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+      : "memory");
+}
+// L2 prefetch of a 3-D tile.
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(c0), "r"(c1),
+               "r"(c2)
+               : "memory");
+}
 // Contiguous global->shared bulk copy (both addresses 16-byte aligned, size a
 // multiple of 16).
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {

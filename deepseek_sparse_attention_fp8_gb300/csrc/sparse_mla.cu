@@ -21,6 +21,7 @@
 // Selected rows are gathered through the block table with 16-byte cp.async;
 // empty or invalid slots are zero-filled and score the sentinel with weight 0.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <cmath>
@@ -38,12 +39,13 @@ constexpr int kThreads = 416;  // warps 0-7 softmax/epilogue, warps 8-11 loads, 
 constexpr int kProdWarp0 = 8;
 constexpr int kMmaWarp = 12;
 constexpr int kTileKeys = 64;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
-constexpr int kMaxSlots = 4096;           // top-k slots one CTA (one split) may cover
-constexpr int kXPitch = 64 * 4 + 16;      // bytes per row of the score-exchange buffer
+constexpr int kMaxSlots = 2048;           // top-k slots one CTA (one split) may cover
+constexpr int kXBufs = 2;                 // score-exchange buffers in flight
+constexpr int kXPitch = 64 * 2 + 16;      // bytes per row of an exchange buffer (fp16 scores)
 
 // kPair: the two CTAs of a cluster split the Dk dims (rank 0: K-blocks
 // [0, kNkb0), rank 1: the rest) and the value dims (rank r: values
@@ -70,7 +72,7 @@ struct MlaSmem {
   static constexpr int kP = kKv + kStages * kKvStage;
   static constexpr int kX = kP + 16384;
   static constexpr int kXBuf = 128 * kXPitch;
-  static constexpr int kRow = kX + (C::kPair ? 2 * kXBuf : 0);
+  static constexpr int kRow = kX + (C::kPair ? kXBufs * kXBuf : 0);
   static constexpr int kLive = kRow + kMaxSlots * 4;
   static constexpr int kCoord = kLive + kStages * kTileKeys;
   static constexpr int kRed = kCoord + kStages * kTileKeys * 4;
@@ -99,6 +101,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+__device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float2 unpack_f16(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+
 __device__ __forceinline__ int find_request(const int32_t* qsl, int B, int t) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {
@@ -119,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t kv_full[kStages], kv_empty[kStages], x_full[2];
+  __shared__ uint64_t kv_full[kStages], kv_empty[kStages], x_full[kXBufs];
   __shared__ uint64_t s_full, s_free, p_full, o_done, q_full, pair_bar[4];
   __shared__ uint32_t tmem_holder;
   __shared__ int s_last_live;
@@ -155,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) mbar_init(&x_full[s], 1);  // local expect_tx; the peer's st.async deliver the bytes
+    for (int s = 0; s < kXBufs; ++s) mbar_init(&x_full[s], 1);  // local expect_tx; the peer's st.async deliver the bytes
     mbar_init(&s_full, 1);
     mbar_init(&s_free, 8);
     mbar_init(&p_full, 8);
@@ -291,11 +302,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     const uint32_t p0s = smem_u32(p_sm);
     auto issue_pv = [&](int i) {
       const int st = i % kStages;
-      const uint32_t v0 = smem_u32(kv_sm + st * L::kKvStage);  // value dims = this CTA's first K-blocks
+      // value dims = this CTA's first K-blocks
+      const uint64_t vd = smem_desc(smem_u32(kv_sm + st * L::kKvStage), L::kKvKb, 1024, kSwizzle128B);
+      const uint64_t pd = smem_desc(p0s, 16, 1024, kSwizzle128B);
 #pragma unroll
       for (int ks = 0; ks < kTileKeys / 16; ++ks)
-        mma_bf16_ss(tmem + kColO, smem_desc(p0s + ks * 32, 16, 1024, kSwizzle128B),
-                    smem_desc(v0 + ks * 2048, L::kKvKb, 1024, kSwizzle128B), idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+        mma_bf16_ss(tmem + kColO, pd + static_cast<uint64_t>((ks * 32) >> 4), vd + static_cast<uint64_t>((ks * 2048) >> 4),
+                    idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
       mma_commit(&kv_empty[st]);
       mma_commit(&o_done);
     };
@@ -309,12 +322,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       }
       tc_fence_after();
       if (lane == 0) {  // this CTA's part of S = Q K^T
-        const uint32_t kv0 = smem_u32(kv_sm + st * L::kKvStage);
-#pragma unroll 1
-        for (int ks = 0; ks < nkb * 4; ++ks)
-          mma_bf16_ts(tmem + kColS, tmem + kColQ + ks * 8,
-                      smem_desc(kv0 + (ks / 4) * L::kKvKb + (ks % 4) * 32, 16, 1024, kSwizzle128B), idesc_qk,
-                      ks > 0 ? 1u : 0u);
+        // descriptors differ only in the start-address field (16-byte units)
+        const uint64_t d0 = smem_desc(smem_u32(kv_sm + st * L::kKvStage), 16, 1024, kSwizzle128B);
+#pragma unroll
+        for (int kb = 0; kb < C::kMaxNkb; ++kb) {
+          if (kb >= nkb) break;
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4)
+            mma_bf16_ts(tmem + kColS, tmem + kColQ + (kb * 4 + k4) * 8,
+                        d0 + static_cast<uint64_t>((kb * L::kKvKb + k4 * 32) >> 4), idesc_qk, (kb | k4) ? 1u : 0u);
+        }
         mma_commit(&s_full);
       }
       __syncwarp();
@@ -347,47 +364,74 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     uint64_t* pbar = &pair_bar[warp & 3];  // joins the two warps of this lane group
     float* red = reinterpret_cast<float*>(smem + L::kRed);  // [parity][key half][128 rows]
     uint32_t x_peer = 0;
-    if constexpr (C::kPair) x_peer = mapa_shared(smem_u32(x_sm + h * kXPitch + kh * 128), static_cast<uint32_t>(r ^ 1));
-    const uint8_t* x_mine = x_sm + h * kXPitch + kh * 128;
-    uint32_t peer_x_full[2] = {0, 0};
+    if constexpr (C::kPair) x_peer = mapa_shared(smem_u32(x_sm + h * kXPitch + kh * 64), static_cast<uint32_t>(r ^ 1));
+    const uint8_t* x_mine = x_sm + h * kXPitch + kh * 64;
+    uint32_t peer_x_full[kXBufs] = {};
     if constexpr (C::kPair) {
-      for (int q = 0; q < 2; ++q) peer_x_full[q] = mapa_shared(smem_u32(&x_full[q]), static_cast<uint32_t>(r ^ 1));
+      for (int q = 0; q < kXBufs; ++q) peer_x_full[q] = mapa_shared(smem_u32(&x_full[q]), static_cast<uint32_t>(r ^ 1));
     }
     float m_ref = kNegSentinel, l_part = 0.f;
-    for (int i = 0; i < n_tiles && !s_abort; ++i) {
-      const int st = i % kStages;
-      if (!mbar_wait(&s_full, i & 1)) {
-        if (lane == 0) abort_now();
-        break;
-      }
-      tc_fence_after();
+    uint32_t prev[16];  // this CTA's fp16 partial scores of the tile waiting for the peer's
+    // The peer's buffer X[i % 2] is free again when tile i is sent: this CTA
+    // has received the peer's tile i-1, which the peer sends only after it has
+    // finished reading X[i % 2] (tile i-2).
+    constexpr int kLag = 0;
+    for (int step = 0; step < n_tiles + kLag && !s_abort; ++step) {
       uint32_t sv[32];
-      tmem_ld32_sync(lane_base + kColS + kh * 32, sv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free);
-      if constexpr (C::kPair) {
-        // swap partial scores with the peer CTA: S = S_rank0 + S_rank1. The
-        // peer's buffer X[i & 1] is free again: this CTA sends tile i only after
-        // receiving the peer's tile i-1, which the peer sends only after it has
-        // finished reading X[i & 1] (tile i-2).
-        const int xp = i & 1;
-        if (tid == 0) mbar_arrive_expect_tx(&x_full[xp], 128 * 64 * 4);  // the peer's whole partial tile
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_async_v4(x_peer + xp * L::kXBuf + c * 16, peer_x_full[xp], sv[4 * c], sv[4 * c + 1], sv[4 * c + 2],
-                      sv[4 * c + 3]);
-        if (!mbar_wait_cluster(&x_full[xp], (i >> 1) & 1)) {
+      uint32_t hv[16];
+      if (step < n_tiles) {
+        if (!mbar_wait(&s_full, step & 1)) {
           if (lane == 0) abort_now();
           break;
         }
+        tc_fence_after();
+        tmem_ld32_sync(lane_base + kColS + kh * 32, sv);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free);
+        if constexpr (C::kPair) {
+          const int xb = step % kXBufs;
+          if (tid == 0) mbar_arrive_expect_tx(&x_full[xb], 128 * 64 * 2);  // the peer's whole partial tile
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 u = *reinterpret_cast<const uint4*>(x_mine + xp * L::kXBuf + c * 16);
-          sv[4 * c] = __float_as_uint(__uint_as_float(sv[4 * c]) + __uint_as_float(u.x));
-          sv[4 * c + 1] = __float_as_uint(__uint_as_float(sv[4 * c + 1]) + __uint_as_float(u.y));
-          sv[4 * c + 2] = __float_as_uint(__uint_as_float(sv[4 * c + 2]) + __uint_as_float(u.z));
-          sv[4 * c + 3] = __float_as_uint(__uint_as_float(sv[4 * c + 3]) + __uint_as_float(u.w));
+          for (int x = 0; x < 16; ++x) hv[x] = pack_f16_sat(__uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]));
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            st_async_v4(x_peer + xb * L::kXBuf + c * 16, peer_x_full[xb], hv[4 * c], hv[4 * c + 1], hv[4 * c + 2],
+                        hv[4 * c + 3]);
+        }
+      }
+      if (step < kLag) {
+#pragma unroll
+        for (int x = 0; x < 16; ++x) prev[x] = hv[x];
+        continue;
+      }
+      const int i = step - kLag;  // the tile finished in this step
+      const int st = i % kStages;
+      if constexpr (C::kPair) {
+        uint32_t cur[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          cur[x] = kLag ? prev[x] : hv[x];
+          prev[x] = hv[x];
+        }
+        const int xb = i % kXBufs;
+        if (!mbar_wait_cluster(&x_full[xb], (i / kXBufs) & 1)) {
+          if (lane == 0) abort_now();
+          break;
+        }
+        // S = own partial + the peer's, both rounded to fp16 for the exchange,
+        // so the two CTAs add the same two values and agree bit for bit
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 u = *reinterpret_cast<const uint4*>(x_mine + xb * L::kXBuf + c * 16);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int y = 0; y < 4; ++y) {
+            const float2 f = unpack_f16(w[y]);
+            const float2 o = unpack_f16(cur[4 * c + y]);
+            sv[8 * c + 2 * y] = __float_as_uint(o.x + f.x);
+            sv[8 * c + 2 * y + 1] = __float_as_uint(o.y + f.y);
+          }
         }
       }
       if (!mbar_wait(&kv_full[st], (i / kStages) & 1)) {  // live flags of this tile

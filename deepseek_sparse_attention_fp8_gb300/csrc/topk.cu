@@ -103,7 +103,20 @@ __device__ void block_select(const float* __restrict__ vals, const int32_t* __re
     return;
   }
   if (kcache != nullptr) {
-    for (int i = tid; i < n; i += kThreads) kcache[i] = make_key(i);
+    // eight independent loads per thread in flight at a time
+    for (int base = 0; base < n; base += 8 * kThreads) {
+      uint32_t kk[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * kThreads + tid;
+        kk[u] = i < n ? make_key(i) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * kThreads + tid;
+        if (i < n) kcache[i] = kk[u];
+      }
+    }
     __syncthreads();
   }
   auto key_at = [&](int i) -> uint32_t { return kcache != nullptr ? kcache[i] : make_key(i); };
