@@ -262,12 +262,9 @@ def main():
     t_idx = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
     t_topk = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
     t_att = [ev[k][2].elapsed_time(ev[k][3]) for k in range(K)]
-    ms = float(np.mean(t_step))
-    if world > 1:
-        tt = torch.tensor([ms], device=step.device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
-    value = world * wl.T / (ms / 1e3)
+    from deepseek_sparse_attention_fp8_gb300.replicas import aggregate
+
+    ms, _, value = aggregate(float(np.mean(t_step)), wl.T, step.device)
 
     # warm-L2 (no flush) for context
     ew = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -302,12 +299,8 @@ def main():
             host_lse.copy_(step.lse, non_blocking=True)
             eve[k][1].record(stream)
         barrier()
-        ms_e2e = float(np.mean([e[0].elapsed_time(e[1]) for e in eve]))
-        if world > 1:
-            tt = torch.tensor([ms_e2e], device=step.device)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            ms_e2e = float(tt.item())
-        e2e = {"value": world * wl.T / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+        ms_e2e, _, v_e2e = aggregate(float(np.mean([e[0].elapsed_time(e[1]) for e in eve])), wl.T, step.device)
+        e2e = {"value": v_e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e}
 
     alg = algorithmic_bytes(wl, step.topk_idx.cpu().numpy())
