@@ -7,19 +7,21 @@
 //   s_i = scale * q[t,h,:] . kv[i,:]          over the selected rows i
 //   out = sum_i softmax(s)_i * kv[i, :Dv]     lse = log sum_i exp(s_i)
 //
-// One CTA handles (token, value half, split). The 128 heads are the MMA M
-// dimension. Per 64-key tile:
-//   S  = Q K^T    tcgen05 kind::f16, M=128 heads, N=64 keys, K=Dk; the first
-//                 384 q dims are the A operand in tensor memory, the rest in
-//                 shared memory;
-//   softmax       thread = head row, lazy rescaling of O (only when the row
-//                 maximum grows by more than 2^8);
-//   O += P V      M=128 heads, N=256 value dims (MN-major view of the same
-//                 shared-memory KV tile), fp32 accumulator in tensor memory.
-// The 512 value dims are split across two CTAs because O for 128 heads x 512
-// dims would fill the whole tensor memory of an SM; both CTAs compute S.
-// Selected rows are gathered through the block table with 16-byte cp.async;
-// empty or invalid slots are zero-filled and score the sentinel with weight 0.
+// The 128 heads are the MMA M dimension. For Dk = 576 a (token, split) is
+// one 2-CTA cluster: CTA r owns K-blocks (64 dims each) [0,4) or [4,9) of
+// every row, gathers only those (4-row TMA gathers through the block table;
+// empty or invalid slots read as zeros and score the sentinel with weight 0),
+// and owns value dims [256r, 256r+256), which are its first four K-blocks.
+// Per 64-key tile, in each CTA:
+//   S_r = Q_r K_r^T   tcgen05 kind::f16, M=128, N=64, A (this CTA's q dims)
+//                     in tensor memory, B from the swizzled KV stage;
+//   exchange          S_r rounded to fp16 goes to the peer over DSMEM
+//                     (st.async); both CTAs form S = f16(S_0) + f16(S_1);
+//   softmax           thread = head row; two warp groups take alternate
+//                     tiles; lazy rescaling of O (only when the row maximum
+//                     grows by more than 2^8);
+//   O_r += P V_r      M=128, N=256, fp32 accumulator in tensor memory.
+// Warp roles: 8 softmax/epilogue warps, 4 producer warps (TMA), 1 MMA warp.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -44,7 +46,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 constexpr int kMaxSlots = 2048;           // top-k slots one CTA (one split) may cover
-constexpr int kXBufs = 2;                 // score-exchange buffers in flight
+constexpr int kXBufs = 2;                 // score-exchange buffers, one per softmax group
+constexpr long long kWaitLimitCycles = 2000000000ll;
+constexpr int kQStage = 2;  // q is staged in KV stages 2 and 3
+static_assert(kMaxSlots <= 256 * 8, "the softmax warps resolve all slots in one pass");
+static_assert(kQStage + 2 <= kStages, "q staging needs two KV stages");
 constexpr int kXPitch = 64 * 2 + 16;      // bytes per row of an exchange buffer (fp16 scores)
 
 // kPair: the two CTAs of a cluster split the Dk dims (rank 0: K-blocks
@@ -76,8 +82,8 @@ struct MlaSmem {
   static constexpr int kLive = kRow + kMaxSlots * 4;
   static constexpr int kCoord = kLive + kStages * kTileKeys;
   static constexpr int kRed = kCoord + kStages * kTileKeys * 4;
-  static constexpr int kTotal = kRed + 2 * 2 * 128 * 4 + 1024;
-  static_assert(C::kMaxNkb * 16384 <= kStages * kKvStage, "q staging does not fit");
+  static constexpr int kTotal = kRed + 6 * 128 * 4 + 1024;
+  static_assert(C::kMaxNkb * 16384 <= 2 * kKvStage, "q staging does not fit in two KV stages");
 };
 
 struct MlaParams {
@@ -130,8 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t kv_full[kStages], kv_empty[kStages], x_full[kXBufs];
-  __shared__ uint64_t s_full, s_free, p_full, o_done, q_full, pair_bar[4];
+  __shared__ uint64_t kv_full[kStages], kv_empty[kStages], x_full[kXBufs], x_empty[kXBufs];
+  // s_full, o_done and m_bar come in pairs indexed by tile parity, so each
+  // softmax group waits on phases of its own tiles only
+  __shared__ uint64_t s_full[2], s_free, p_full, o_done[2], o_final, q_full, q_ready, rows_ready, m_bar[2], epi_bar;
   __shared__ uint32_t tmem_holder;
   __shared__ int s_last_live;
   __shared__ volatile int s_abort;
@@ -158,21 +166,41 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   uint8_t* p_sm = smem + L::kP;
   uint8_t* x_sm = smem + L::kX;
   int* row_sm = reinterpret_cast<int*>(smem + L::kRow);
-  uint8_t* live_sm = smem + L::kLive;
+  uint16_t* live_m = reinterpret_cast<uint16_t*>(smem + L::kLive);  // [stage][producer warp]: live-key bits
   int* coord_sm = reinterpret_cast<int*>(smem + L::kCoord);
+
+  // the softmax warps load their top-k slots before anything else
+  const int32_t* idx_row = p.topk + static_cast<int64_t>(t) * p.K + slot0;
+  int idx[8];
+  if (warp < 8) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int sl = u * 256 + tid;
+      idx[u] = sl < n_slots ? __ldg(idx_row + sl) : -1;
+    }
+  }
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_full[s], 4);  // the four producer warps
       mbar_init(&kv_empty[s], 1);
     }
-    for (int s = 0; s < kXBufs; ++s) mbar_init(&x_full[s], 1);  // local expect_tx; the peer's st.async deliver the bytes
-    mbar_init(&s_full, 1);
-    mbar_init(&s_free, 8);
-    mbar_init(&p_full, 8);
-    mbar_init(&o_done, 1);
+    for (int s = 0; s < kXBufs; ++s) {
+      mbar_init(&x_full[s], 1);   // local expect_tx; the peer's st.async deliver the bytes
+      mbar_init(&x_empty[s], 4);  // the peer's four reading warps, remotely
+    }
+    mbar_init(&s_free, 4);
+    mbar_init(&p_full, 4);
+    mbar_init(&o_final, 1);
     mbar_init(&q_full, 1);
-    for (int q = 0; q < 4; ++q) mbar_init(&pair_bar[q], 64);
+    mbar_init(&q_ready, 8);
+    mbar_init(&rows_ready, 8);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&s_full[q], 1);
+      mbar_init(&o_done[q], 1);
+      mbar_init(&m_bar[q], 4);
+    }
+    mbar_init(&epi_bar, 256);
     fence_mbar_init();
     s_last_live = -1;
     s_abort = 0;
@@ -195,47 +223,44 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     report(p.dev_status, DSA_DEVERR_TIMEOUT);
   };
 
-  // ---- prologue: this CTA's q K-blocks by TMA into the idle KV stage area;
-  // the softmax warps resolve the split's top-k slots to physical rows
+  // ---- prologue: this CTA's q K-blocks go by TMA into KV stages kQStage..,
+  // which tiles 0 and 1 leave untouched, so the producers start gathering as
+  // soon as the slots are resolved, while q moves on into tensor memory
+  uint8_t* q_stage = kv_sm + kQStage * L::kKvStage;
   if (tid == kProdWarp0 * 32) {  // first producer thread
     prefetch_tmap(&qmap);
     prefetch_tmap(&kvmap);
     mbar_arrive_expect_tx(&q_full, nkb * 16384);
     for (int kb = 0; kb < nkb; ++kb)
-      tma_load_3d(smem_u32(kv_sm + kb * 16384), &qmap, &q_full, (kb0 + kb) * 64, 0, t);
+      tma_load_3d(smem_u32(q_stage + kb * 16384), &qmap, &q_full, (kb0 + kb) * 64, 0, t);
   }
   if (warp < 8) {
+    // the split's top-k slots -> physical rows (-1: empty or invalid)
     const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-    const int32_t* idx_row = p.topk + static_cast<int64_t>(t) * p.K + slot0;
+    int blk[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      blk[u] = (idx[u] >= 0 && idx[u] < valid) ? __ldg(bt_row + idx[u] / p.block_size) : -1;
     int last = -1;
-    for (int base = 0; base < n_slots; base += 256 * 8) {
-      int idx[8], blk[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int sl = base + u * 256 + tid;
-        idx[u] = sl < n_slots ? __ldg(idx_row + sl) : -1;
+    for (int u = 0; u < 8; ++u) {
+      const int sl = u * 256 + tid;
+      if (sl >= n_slots) continue;
+      int row = -1;
+      if (idx[u] >= 0 && idx[u] < valid) {
+        if (blk[u] >= 0 && blk[u] < p.num_blocks)
+          row = blk[u] * p.rows_per_block + idx[u] % p.block_size;
+        else if (r == 0)
+          report(p.dev_status, DSA_DEVERR_BLOCK_OOB);
+      } else if (idx[u] != -1 && r == 0) {
+        report(p.dev_status, DSA_DEVERR_INDEX_OOB);
       }
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        blk[u] = (idx[u] >= 0 && idx[u] < valid) ? __ldg(bt_row + idx[u] / p.block_size) : -1;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int sl = base + u * 256 + tid;
-        if (sl >= n_slots) continue;
-        int row = -1;
-        if (idx[u] >= 0 && idx[u] < valid) {
-          if (blk[u] >= 0 && blk[u] < p.num_blocks)
-            row = blk[u] * p.rows_per_block + idx[u] % p.block_size;
-          else if (r == 0)
-            report(p.dev_status, DSA_DEVERR_BLOCK_OOB);
-        } else if (idx[u] != -1 && r == 0) {
-          report(p.dev_status, DSA_DEVERR_INDEX_OOB);
-        }
-        row_sm[sl] = row;
-        if (row >= 0) last = sl;
-      }
+      row_sm[sl] = row;
+      if (row >= 0) last = sl;
     }
     if (last >= 0) atomicMax(&s_last_live, last);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rows_ready);
     // this CTA's q dims -> tensor memory (A operand of QK)
     if (!mbar_wait(&q_full, 0)) {
       if (lane == 0) abort_now();
@@ -249,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
         for (int half = 0; half < 2; ++half) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const uint4 u = *reinterpret_cast<const uint4*>(kv_sm + kb * 16384 + sw128_offset(hq, half * 4 + c));
+            const uint4 u = *reinterpret_cast<const uint4*>(q_stage + kb * 16384 + sw128_offset(hq, half * 4 + c));
             v[4 * c] = u.x;
             v[4 * c + 1] = u.y;
             v[4 * c + 2] = u.z;
@@ -259,12 +284,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
         }
       }
       tmem_st_wait();
-      fence_proxy_async_smem();  // the staging area is refilled by TMA next
+      fence_proxy_async_smem();  // the staging stages are refilled by TMA next
     }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&q_ready);
   }
-  tc_fence_before();
-  __syncthreads();  // q in place, slots resolved, staging area free
-  tc_fence_after();
+  if (!mbar_wait(&rows_ready, 0) && lane == 0) abort_now();
   const int n_tiles = s_abort ? 0 : (s_last_live + kTileKeys) / kTileKeys;
 
   if (warp >= kProdWarp0 && warp < kMmaWarp) {
@@ -272,35 +298,70 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     // this CTA's K-blocks only
     const int pw = warp - kProdWarp0;
     const uint32_t tile_bytes = kTileKeys * nkb * 128;
+    int issued = 0;
     for (int i = 0; i < n_tiles && !s_abort; ++i) {
       const int st = i % kStages;
       if (i >= kStages && !mbar_wait(&kv_empty[st], ((i / kStages) - 1) & 1)) {
         if (lane == 0) abort_now();
         break;
       }
+      if (i == kQStage && !mbar_wait(&q_ready, 0)) {  // q has left its staging stages
+        if (lane == 0) abort_now();
+        break;
+      }
+      bool live = false;
       if (lane < 16) {
         const int kr = pw * 16 + lane;
         const int sl = i * kTileKeys + kr;
         const int row = sl < n_slots ? row_sm[sl] : -1;
-        live_sm[st * kTileKeys + kr] = row >= 0 ? 1 : 0;
-        coord_sm[st * kTileKeys + kr] = row >= 0 ? row : p.total_rows;  // out of range: zero fill
+        live = row >= 0;
+        coord_sm[st * kTileKeys + kr] = live ? row : p.total_rows;  // out of range: zero fill
       }
+      const uint32_t mask = __ballot_sync(0xFFFFFFFFu, live);
+      if (lane == 0) live_m[st * 4 + pw] = static_cast<uint16_t>(mask);
       __syncwarp();
-      if (pw == 0 && lane == 0) mbar_arrive_expect_tx(&kv_full[st], tile_bytes);
+      if (lane == 0) {
+        if (pw == 0) mbar_arrive_expect_tx(&kv_full[st], tile_bytes);
+        else mbar_arrive(&kv_full[st]);
+      }
       if (lane < 4 * nkb) {
         const int g = pw * 4 + (lane & 3), kb = lane >> 2;
         const int* cs = coord_sm + st * kTileKeys + 4 * g;
         tma_gather4(smem_u32(kv_sm + st * L::kKvStage + kb * L::kKvKb + g * 512), &kvmap, &kv_full[st],
                     (kb0 + kb) * 64, cs[0], cs[1], cs[2], cs[3]);
       }
+      issued = i + 1;
     }
+    if (s_abort && pw == 0) {
+      // let the gathers in flight land before shared memory is given up
+      for (int i = max(0, issued - kStages); i < issued; ++i)
+        mbar_wait(&kv_full[i % kStages], (i / kStages) & 1, 20000000ll);
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   } else if (warp == kMmaWarp) {
-    // ---------------- MMA issuer
-    if (!mbar_wait(&q_full, 0) && lane == 0) abort_now();
+    // ---------------- MMA issuer. QK of tile i needs its KV stage and S of
+    // tile i-1 read out; PV of tile i needs P of tile i. The two softmax
+    // groups finish their tiles out of step, so whichever is ready goes first.
+    if (!mbar_wait(&q_ready, 0) && lane == 0) abort_now();
+    tc_fence_after();
     const uint32_t idesc_qk = idesc_bf16(128, kTileKeys, false, false);
     const uint32_t idesc_pv = idesc_bf16(128, C::kDvc, false, true);
     const uint32_t p0s = smem_u32(p_sm);
-    auto issue_pv = [&](int i) {
+    auto issue_qk = [&](int i) {  // this CTA's part of S = Q K^T
+      const int st = i % kStages;
+      // descriptors differ only in the start-address field (16-byte units)
+      const uint64_t d0 = smem_desc(smem_u32(kv_sm + st * L::kKvStage), 16, 1024, kSwizzle128B);
+#pragma unroll
+      for (int kb = 0; kb < C::kMaxNkb; ++kb) {
+        if (kb >= nkb) break;
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4)
+          mma_bf16_ts(tmem + kColS, tmem + kColQ + (kb * 4 + k4) * 8,
+                      d0 + static_cast<uint64_t>((kb * L::kKvKb + k4 * 32) >> 4), idesc_qk, (kb | k4) ? 1u : 0u);
+      }
+      mma_commit(&s_full[i & 1]);
+    };
+    auto issue_pv = [&](int i) {  // O += P V
       const int st = i % kStages;
       // value dims = this CTA's first K-blocks
       const uint64_t vd = smem_desc(smem_u32(kv_sm + st * L::kKvStage), L::kKvKb, 1024, kSwizzle128B);
@@ -310,192 +371,191 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
         mma_bf16_ss(tmem + kColO, pd + static_cast<uint64_t>((ks * 32) >> 4), vd + static_cast<uint64_t>((ks * 2048) >> 4),
                     idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
       mma_commit(&kv_empty[st]);
-      mma_commit(&o_done);
+      mma_commit(&o_done[i & 1]);
+      if (i == n_tiles - 1) mma_commit(&o_final);
     };
-    for (int i = 0; i < n_tiles && !s_abort; ++i) {
+    int nq = 0, np = 0;  // next tile to issue QK / PV for
+    long long idle_since = clock64();
+    while (np < n_tiles && !s_abort) {
+      bool progressed = false;
+      if (nq < n_tiles) {
+        const int st = nq % kStages;
+        bool ready = mbar_test_wait(&kv_full[st], (nq / kStages) & 1) &&
+                     (nq == 0 || mbar_test_wait(&s_free, (nq - 1) & 1));
+        ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+        if (ready) {
+          tc_fence_after();
+          if (lane == 0) issue_qk(nq);
+          __syncwarp();
+          ++nq;
+          progressed = true;
+        }
+      }
+      if (np < nq) {
+        const bool ready = __shfl_sync(0xFFFFFFFFu, mbar_test_wait(&p_full, np & 1), 0);
+        if (ready) {
+          tc_fence_after();
+          if (lane == 0) issue_pv(np);
+          __syncwarp();
+          ++np;
+          progressed = true;
+        }
+      }
+      if (progressed) {
+        idle_since = clock64();
+      } else if (clock64() - idle_since > kWaitLimitCycles) {
+        if (lane == 0) abort_now();
+        break;
+      } else {
+        __nanosleep(20);
+      }
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  } else {
+    // ---------------- softmax: group g = warp / 4 takes the tiles i with
+    // i % 2 == g, so the score exchange and loads of one tile overlap the
+    // arithmetic of the other; thread = head row h (its TMEM lane), all 64
+    // keys of a tile. The running maximum passes from group to group through
+    // shared memory, tile by tile.
+    const int g = warp >> 2;
+    const int h = (warp & 3) * 32 + lane;
+    const bool leader = (tid & 127) == 0;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    float* m_hand = reinterpret_cast<float*>(smem + L::kRed);  // [group][row]: m after the group's latest tile
+    const uint8_t* x_mine = x_sm + g * L::kXBuf + h * kXPitch;
+    uint32_t x_peer = 0, peer_x_full = 0, peer_x_empty = 0;
+    if constexpr (C::kPair) {
+      x_peer = mapa_shared(smem_u32(x_mine), static_cast<uint32_t>(r ^ 1));
+      peer_x_full = mapa_shared(smem_u32(&x_full[g]), static_cast<uint32_t>(r ^ 1));
+      peer_x_empty = mapa_shared(smem_u32(&x_empty[g]), static_cast<uint32_t>(r ^ 1));
+    }
+    float m_own = kNegSentinel, l_part = 0.f;  // l_part is expressed against m_own
+    for (int i = g; i < n_tiles && !s_abort; i += 2) {
+      const int u = i >> 1;  // tiles this group has finished
       const int st = i % kStages;
-      bool ok = mbar_wait(&kv_full[st], (i / kStages) & 1);
-      if (ok && i >= 1) ok = mbar_wait(&s_free, (i - 1) & 1);
-      if (!ok) {
+      float s[kTileKeys];
+      if (!mbar_wait(&s_full[g], u & 1)) {
         if (lane == 0) abort_now();
         break;
       }
       tc_fence_after();
-      if (lane == 0) {  // this CTA's part of S = Q K^T
-        // descriptors differ only in the start-address field (16-byte units)
-        const uint64_t d0 = smem_desc(smem_u32(kv_sm + st * L::kKvStage), 16, 1024, kSwizzle128B);
+      if constexpr (C::kPair) {
+        // this CTA's partial scores, rounded to fp16, go to the peer; both
+        // CTAs then add the same two fp16 partials and agree bit for bit
+        uint32_t hv[32];
 #pragma unroll
-        for (int kb = 0; kb < C::kMaxNkb; ++kb) {
-          if (kb >= nkb) break;
+        for (int half = 0; half < 2; ++half) {
+          uint32_t sv[32];
+          tmem_ld32_sync(lane_base + kColS + half * 32, sv);
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4)
-            mma_bf16_ts(tmem + kColS, tmem + kColQ + (kb * 4 + k4) * 8,
-                        d0 + static_cast<uint64_t>((kb * L::kKvKb + k4 * 32) >> 4), idesc_qk, (kb | k4) ? 1u : 0u);
+          for (int x = 0; x < 16; ++x)
+            hv[half * 16 + x] = pack_f16_sat(__uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]));
         }
-        mma_commit(&s_full);
-      }
-      __syncwarp();
-      if (i >= 1) {  // O += P V for the previous tile
-        if (!mbar_wait(&p_full, (i - 1) & 1)) {
-          if (lane == 0) abort_now();
-          break;
-        }
-        tc_fence_after();
-        if (lane == 0) issue_pv(i - 1);
-        __syncwarp();
-      }
-    }
-    if (n_tiles > 0 && !s_abort) {
-      const int i = n_tiles - 1;
-      if (!mbar_wait(&p_full, i & 1)) {
-        if (lane == 0) abort_now();
-      } else {
-        tc_fence_after();
-        if (lane == 0) issue_pv(i);
-        __syncwarp();
-      }
-    }
-  } else {
-    // ---------------- softmax: warps w and w+4 share TMEM lanes 32*(w%4).. (one
-    // head row per thread) and take keys [32*kh, 32*kh+32) of each tile
-    const int kh = warp >> 2;            // key half
-    const int h = (warp & 3) * 32 + lane;  // head row
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    uint64_t* pbar = &pair_bar[warp & 3];  // joins the two warps of this lane group
-    float* red = reinterpret_cast<float*>(smem + L::kRed);  // [parity][key half][128 rows]
-    uint32_t x_peer = 0;
-    if constexpr (C::kPair) x_peer = mapa_shared(smem_u32(x_sm + h * kXPitch + kh * 64), static_cast<uint32_t>(r ^ 1));
-    const uint8_t* x_mine = x_sm + h * kXPitch + kh * 64;
-    uint32_t peer_x_full[kXBufs] = {};
-    if constexpr (C::kPair) {
-      for (int q = 0; q < kXBufs; ++q) peer_x_full[q] = mapa_shared(smem_u32(&x_full[q]), static_cast<uint32_t>(r ^ 1));
-    }
-    float m_ref = kNegSentinel, l_part = 0.f;
-    uint32_t prev[16];  // this CTA's fp16 partial scores of the tile waiting for the peer's
-    // The peer's buffer X[i % 2] is free again when tile i is sent: this CTA
-    // has received the peer's tile i-1, which the peer sends only after it has
-    // finished reading X[i % 2] (tile i-2).
-    constexpr int kLag = 0;
-    for (int step = 0; step < n_tiles + kLag && !s_abort; ++step) {
-      uint32_t sv[32];
-      uint32_t hv[16];
-      if (step < n_tiles) {
-        if (!mbar_wait(&s_full, step & 1)) {
-          if (lane == 0) abort_now();
-          break;
-        }
-        tc_fence_after();
-        tmem_ld32_sync(lane_base + kColS + kh * 32, sv);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free);
-        if constexpr (C::kPair) {
-          const int xb = step % kXBufs;
-          if (tid == 0) mbar_arrive_expect_tx(&x_full[xb], 128 * 64 * 2);  // the peer's whole partial tile
-#pragma unroll
-          for (int x = 0; x < 16; ++x) hv[x] = pack_f16_sat(__uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]));
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            st_async_v4(x_peer + xb * L::kXBuf + c * 16, peer_x_full[xb], hv[4 * c], hv[4 * c + 1], hv[4 * c + 2],
-                        hv[4 * c + 3]);
-        }
-      }
-      if (step < kLag) {
-#pragma unroll
-        for (int x = 0; x < 16; ++x) prev[x] = hv[x];
-        continue;
-      }
-      const int i = step - kLag;  // the tile finished in this step
-      const int st = i % kStages;
-      if constexpr (C::kPair) {
-        uint32_t cur[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          cur[x] = kLag ? prev[x] : hv[x];
-          prev[x] = hv[x];
-        }
-        const int xb = i % kXBufs;
-        if (!mbar_wait_cluster(&x_full[xb], (i / kXBufs) & 1)) {
+        // the peer has read what this group sent for its previous tile (its
+        // reads completed before its arrival, so no acquire is needed here)
+        if (u >= 1 && !mbar_wait(&x_empty[g], (u - 1) & 1)) {
           if (lane == 0) abort_now();
           break;
         }
-        // S = own partial + the peer's, both rounded to fp16 for the exchange,
-        // so the two CTAs add the same two values and agree bit for bit
+        if (leader) mbar_arrive_expect_tx(&x_full[g], 128 * kTileKeys * 2);  // the peer's whole partial tile
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 u = *reinterpret_cast<const uint4*>(x_mine + xb * L::kXBuf + c * 16);
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        for (int c = 0; c < 8; ++c)
+          st_async_v4(x_peer + c * 16, peer_x_full, hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
+        if (!mbar_wait_cluster(&x_full[g], u & 1)) {
+          if (lane == 0) abort_now();
+          break;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 w4 = *reinterpret_cast<const uint4*>(x_mine + c * 16);
+          const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
           for (int y = 0; y < 4; ++y) {
             const float2 f = unpack_f16(w[y]);
-            const float2 o = unpack_f16(cur[4 * c + y]);
-            sv[8 * c + 2 * y] = __float_as_uint(o.x + f.x);
-            sv[8 * c + 2 * y + 1] = __float_as_uint(o.y + f.y);
+            const float2 o = unpack_f16(hv[4 * c + y]);
+            s[8 * c + 2 * y] = o.x + f.x;
+            s[8 * c + 2 * y + 1] = o.y + f.y;
           }
         }
+        // the loaded values are consumed above, so the loads have completed
+        // when the (fence-free) arrival tells the peer it may overwrite them
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_relaxed(peer_x_empty);
+      } else {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t sv[32];
+          tmem_ld32_sync(lane_base + kColS + half * 32, sv);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) s[half * 32 + x] = __uint_as_float(sv[x]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free);
       }
-      if (!mbar_wait(&kv_full[st], (i / kStages) & 1)) {  // live flags of this tile
+      if (!mbar_wait(&kv_full[st], (i / kStages) & 1)) {  // orders the producers' live masks
         if (lane == 0) abort_now();
         break;
       }
-      const uint32_t* lw = reinterpret_cast<const uint32_t*>(live_sm + st * kTileKeys + kh * 32);
-      uint32_t live_bits = 0;
+      const uint64_t live = *reinterpret_cast<const uint64_t*>(live_m + st * 4);
+      float mt = -INFINITY;  // the tile's raw row maximum (scale > 0)
 #pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        const uint32_t w4 = lw[x];
-#pragma unroll
-        for (int y = 0; y < 4; ++y) live_bits |= ((w4 >> (8 * y)) & 1u) << (4 * x + y);
+      for (int x = 0; x < kTileKeys; ++x) {
+        if (!((live >> x) & 1u)) s[x] = -INFINITY;
+        mt = fmaxf(mt, s[x]);
       }
-      float mt = kNegSentinel;
+      float m_prev = kNegSentinel;  // what O and the other group's sum are expressed against
+      if (i >= 1) {
+        if (!mbar_wait(&m_bar[g ^ 1], ((i - 1) >> 1) & 1)) {
+          if (lane == 0) abort_now();
+          break;
+        }
+        m_prev = m_hand[(g ^ 1) * 128 + h];
+      }
+      const float mt2 = mt * p.scale_log2;
+      const bool rescale = mt2 > m_prev + kRescaleThreshold;
+      const float m_new = rescale ? mt2 : m_prev;
+      m_hand[g * 128 + h] = m_new;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m_bar[g]);
+      // masked keys are -inf here and get weight exactly 0
+      const float neg_m = -m_new;
+      uint32_t pw[32];
+      float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
       for (int x = 0; x < 32; ++x) {
-        const float s = ((live_bits >> x) & 1u) ? __uint_as_float(sv[x]) * p.scale_log2 : kNegSentinel;
-        sv[x] = __float_as_uint(s);
-        mt = fmaxf(mt, s);
-      }
-      // the row maximum over both key halves (slots alternate by tile parity, so
-      // one join per tile suffices)
-      red[(i & 1) * 256 + kh * 128 + h] = mt;
-      mbar_arrive(pbar);
-      if (!mbar_wait(pbar, i & 1)) {
-        if (lane == 0) abort_now();
-        break;
-      }
-      mt = fmaxf(mt, red[(i & 1) * 256 + (kh ^ 1) * 128 + h]);
-      float alpha = 1.f;
-      const bool rescale = mt > m_ref + kRescaleThreshold;
-      if (rescale) {
-        alpha = ex2_approx(m_ref - mt);
-        m_ref = mt;
-        l_part *= alpha;
-      }
-      uint32_t pw[16];
-      float psum = 0.f;
-#pragma unroll
-      for (int x = 0; x < 16; ++x) {
-        const float a = ((live_bits >> (2 * x)) & 1u) ? ex2_approx(__uint_as_float(sv[2 * x]) - m_ref) : 0.f;
-        const float c = ((live_bits >> (2 * x + 1)) & 1u) ? ex2_approx(__uint_as_float(sv[2 * x + 1]) - m_ref) : 0.f;
+        const float a = ex2_approx(fmaf(s[2 * x], p.scale_log2, neg_m));
+        const float c = ex2_approx(fmaf(s[2 * x + 1], p.scale_log2, neg_m));
         const __nv_bfloat162 pb = __floats2bfloat162_rn(a, c);
         // the normaliser sums the bf16 weights that the PV product uses
-        psum += __bfloat162float(pb.x) + __bfloat162float(pb.y);
+        ps0 += __bfloat162float(pb.x);
+        ps1 += __bfloat162float(pb.y);
         pw[x] = *reinterpret_cast<const uint32_t*>(&pb);
       }
-      l_part += psum;
+      if (m_new != m_own) {
+        l_part *= ex2_approx(m_own - m_new);
+        m_own = m_new;
+      }
+      l_part += ps0 + ps1;
       // P and O are free once PV of the previous tile is done
       if (i >= 1) {
-        if (!mbar_wait(&o_done, (i - 1) & 1)) {
+        if (!mbar_wait(&o_done[g ^ 1], ((i - 1) >> 1) & 1)) {
           if (lane == 0) abort_now();
           break;
         }
         tc_fence_after();
       }
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(p_sm + sw128_offset(h, kh * 4 + c)) =
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(p_sm + sw128_offset(h, c)) =
             make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-      if (i >= 1 && __any_sync(0xFFFFFFFFu, rescale)) {  // each warp of the pair scales half of O
+      if (i >= 1 && __any_sync(0xFFFFFFFFu, rescale)) {
+        const float alpha = rescale ? ex2_approx(m_prev - m_new) : 1.f;
 #pragma unroll 1
-        for (int c = kh * (C::kDvc / 2); c < (kh + 1) * (C::kDvc / 2); c += 32) {
+        for (int c = 0; c < C::kDvc; c += 32) {
           uint32_t o[32];
           tmem_ld32_sync(lane_base + kColO + c, o);
 #pragma unroll
@@ -510,22 +570,25 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       if (lane == 0) mbar_arrive(&p_full);
     }
 
-    // ---- epilogue: l = l_half0 + l_half1; each warp of the pair writes half of the columns
+    // ---- epilogue: both groups' sums against the final maximum (the larger
+    // of the two, as the maximum only grows); each group writes half of this
+    // CTA's value columns
+    float* epi = m_hand + 2 * 128;  // [group][m, l][row]
+    epi[(2 * g) * 128 + h] = m_own;
+    epi[(2 * g + 1) * 128 + h] = l_part;
     bool o_valid = n_tiles > 0 && !s_abort;
-    float l_sum = 0.f;
-    {
-      const int e = n_tiles & 1;  // the join after the last tile
-      red[e * 256 + kh * 128 + h] = l_part;
-      mbar_arrive(pbar);
-      if (mbar_wait(pbar, n_tiles & 1)) {
-        l_sum = red[e * 256 + h] + red[e * 256 + 128 + h];
-      } else {
-        if (lane == 0) abort_now();
-        o_valid = false;
-      }
+    float m_fin = kNegSentinel, l_sum = 0.f;
+    mbar_arrive(&epi_bar);
+    if (mbar_wait(&epi_bar, 0)) {
+      const float m0 = epi[h], l0 = epi[128 + h], m1 = epi[256 + h], l1 = epi[384 + h];
+      m_fin = fmaxf(m0, m1);
+      l_sum = l0 * ex2_approx(m0 - m_fin) + l1 * ex2_approx(m1 - m_fin);
+    } else {
+      if (lane == 0) abort_now();
+      o_valid = false;
     }
     if (o_valid) {
-      if (!mbar_wait(&o_done, (n_tiles - 1) & 1)) {
+      if (!mbar_wait(&o_final, 0)) {
         if (lane == 0) abort_now();
         o_valid = false;
       }
@@ -533,44 +596,66 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     o_valid = __all_sync(0xFFFFFFFFu, o_valid) && !s_abort;
     tc_fence_after();
     const bool have = o_valid && l_sum > 0.f;
+    // the merge grid (if any) may launch now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Write-out through shared memory (the KV stages are idle now): each
+    // thread stages its row's half of this CTA's value columns, then each
+    // warp stores its 32 rows as contiguous segments, 16 bytes per lane.
     constexpr int kHalf = C::kDvc / 2;
-    if (p.splits == 1) {
+    constexpr int kPitch = kHalf * 4 + 16;  // staged row: fp32 or bf16 values + pad
+    static_assert(8 * 32 * kPitch <= kStages * L::kKvStage, "write-out staging does not fit");
+    const bool final_out = p.splits == 1;  // bf16 output, else fp32 partials
+    uint8_t* stg = kv_sm + warp * 32 * kPitch;
+    {
       const float inv = have ? 1.f / l_sum : 0.f;
-      uint16_t* dst = p.out + (static_cast<int64_t>(t) * p.H + h) * DV + r * C::kDvc;
+      uint8_t* srow = stg + lane * kPitch;
 #pragma unroll 1
-      for (int c = kh * kHalf; c < (kh + 1) * kHalf; c += 32) {
+      for (int c = 0; c < kHalf; c += 32) {
         uint32_t o[32];
-        if (o_valid) tmem_ld32_sync(lane_base + kColO + c, o);
-        if (h < p.H) {
-          uint32_t w[16];
+        if (o_valid) tmem_ld32_sync(lane_base + kColO + g * kHalf + c, o);
+        if (final_out) {
+          uint4* d = reinterpret_cast<uint4*>(srow + c * 2);
 #pragma unroll
-          for (int x = 0; x < 16; ++x)
-            w[x] = have ? pack_bf16(__uint_as_float(o[2 * x]) * inv, __uint_as_float(o[2 * x + 1]) * inv) : 0u;
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+          for (int x = 0; x < 4; ++x) {
+            uint32_t w[4];
 #pragma unroll
-          for (int x = 0; x < 4; ++x) d4[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
-        }
-      }
-      if (r == 0 && kh == 0 && h < p.H && p.lse != nullptr)
-        p.lse[static_cast<int64_t>(t) * p.H + h] = have ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
-    } else {
-      const int64_t row = (static_cast<int64_t>(t) * p.H + h) * p.splits + j;
-      float* dst = p.o_part + row * DV + r * C::kDvc;
-#pragma unroll 1
-      for (int c = kh * kHalf; c < (kh + 1) * kHalf; c += 32) {
-        uint32_t o[32];
-        if (o_valid) tmem_ld32_sync(lane_base + kColO + c, o);
-        if (h < p.H) {
-          float4* d4 = reinterpret_cast<float4*>(dst + c);
+            for (int y = 0; y < 4; ++y)
+              w[y] = have ? pack_bf16(__uint_as_float(o[8 * x + 2 * y]) * inv, __uint_as_float(o[8 * x + 2 * y + 1]) * inv)
+                          : 0u;
+            d[x] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+          uint4* d = reinterpret_cast<uint4*>(srow + c * 4);
 #pragma unroll
           for (int x = 0; x < 8; ++x)
-            d4[x] = o_valid ? make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
-                                          __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3]))
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
+            d[x] = o_valid ? make_uint4(o[4 * x], o[4 * x + 1], o[4 * x + 2], o[4 * x + 3]) : make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      if (r == 0 && kh == 0 && h < p.H)
-        p.ml_part[row] = make_float2(o_valid ? m_ref : kNegSentinel, o_valid ? l_sum : 0.f);
+    }
+    __syncwarp();
+    {
+      const int chunks = final_out ? kHalf * 2 / 16 : kHalf * 4 / 16;  // 16-byte chunks per row segment
+      const int rbase = (warp & 3) * 32;
+#pragma unroll 4
+      for (int e = lane; e < 32 * chunks; e += 32) {
+        const int rr = e / chunks, ch = e - rr * chunks;
+        const int hh = rbase + rr;
+        if (hh >= p.H) continue;
+        const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * kPitch + ch * 16);
+        const int64_t row = static_cast<int64_t>(t) * p.H + hh;
+        uint8_t* gdst = final_out
+                            ? reinterpret_cast<uint8_t*>(p.out + row * DV + r * C::kDvc + g * kHalf)
+                            : reinterpret_cast<uint8_t*>(p.o_part + (row * p.splits + j) * DV + r * C::kDvc + g * kHalf);
+        *reinterpret_cast<uint4*>(gdst + ch * 16) = v;
+      }
+    }
+    if (r == 0 && g == 0 && h < p.H) {
+      const int64_t row = static_cast<int64_t>(t) * p.H + h;
+      if (final_out) {
+        if (p.lse != nullptr) p.lse[row] = have ? (m_fin + log2f(l_sum)) * kLn2 : -INFINITY;
+      } else {
+        p.ml_part[row * p.splits + j] = make_float2(o_valid ? m_fin : kNegSentinel, o_valid ? l_sum : 0.f);
+      }
     }
   }
 
@@ -582,32 +667,65 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
 }
 
 // a4: out = sum_j 2^(m_j-M) o_j / sum_j 2^(m_j-M) l_j, M = max_j m_j (log2 units).
+// A thread merges 8 consecutive values of one (token, head) row; a block of
+// 128 threads covers 128 * 8 / DV rows. Launched as a programmatic dependent
+// of the split kernel: it waits for that grid's completion before any read.
 __global__ void __launch_bounds__(128) mla_merge_kernel(const float* __restrict__ o_part,
-                                                        const float2* __restrict__ ml, int S, int DV,
+                                                        const float2* __restrict__ ml, int S, int DV, int64_t n_rows,
                                                         uint16_t* __restrict__ out, float* __restrict__ lse) {
-  const int64_t row = blockIdx.x;  // t * H + h
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int tpr = DV / 8;  // threads per row
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (128 / tpr) + threadIdx.x / tpr;
+  if (row >= n_rows) return;
+  const int v = (threadIdx.x % tpr) * 8;
   const float2* mlr = ml + row * S;
   float M = kNegSentinel;
   for (int j = 0; j < S; ++j) M = fmaxf(M, mlr[j].x);
   float den = 0.f;
-  for (int j = 0; j < S; ++j) den += exp2f(mlr[j].x - M) * mlr[j].y;
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  for (int v = threadIdx.x * 4; v < DV; v += blockDim.x * 4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < S; ++j) {
-      const float a = exp2f(mlr[j].x - M);
-      const float4 o = *reinterpret_cast<const float4*>(o_part + (row * S + j) * DV + v);
-      acc.x = fmaf(a, o.x, acc.x);
-      acc.y = fmaf(a, o.y, acc.y);
-      acc.z = fmaf(a, o.z, acc.z);
-      acc.w = fmaf(a, o.w, acc.w);
-    }
-    uint2 w;
-    w.x = pack_bf16(acc.x * inv, acc.y * inv);
-    w.y = pack_bf16(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(out + row * DV + v) = w;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const float* orow = o_part + row * S * DV + v;
+#pragma unroll 4
+  for (int j = 0; j < S; ++j) {
+    const float2 mlj = mlr[j];
+    const float a = exp2f(mlj.x - M);
+    den = fmaf(a, mlj.y, den);
+    const float4 o0 = *reinterpret_cast<const float4*>(orow + static_cast<int64_t>(j) * DV);
+    const float4 o1 = *reinterpret_cast<const float4*>(orow + static_cast<int64_t>(j) * DV + 4);
+    acc[0] = fmaf(a, o0.x, acc[0]);
+    acc[1] = fmaf(a, o0.y, acc[1]);
+    acc[2] = fmaf(a, o0.z, acc[2]);
+    acc[3] = fmaf(a, o0.w, acc[3]);
+    acc[4] = fmaf(a, o1.x, acc[4]);
+    acc[5] = fmaf(a, o1.y, acc[5]);
+    acc[6] = fmaf(a, o1.z, acc[6]);
+    acc[7] = fmaf(a, o1.w, acc[7]);
   }
-  if (threadIdx.x == 0 && lse != nullptr) lse[row] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  uint4 w;
+  w.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+  w.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+  w.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+  w.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+  *reinterpret_cast<uint4*>(out + row * DV + v) = w;
+  if (v == 0 && lse != nullptr) lse[row] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
+}
+
+dsa_status_t launch_merge(const MlaParams& p, int Dv, float* lse, cudaStream_t s) {
+  const int64_t n_rows = static_cast<int64_t>(p.T) * p.H;
+  const int rows_per_block = 128 / (Dv / 8);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((n_rows + rows_per_block - 1) / rows_per_block));
+  cfg.blockDim = dim3(128);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, mla_merge_kernel, static_cast<const float*>(p.o_part),
+                                     static_cast<const float2*>(p.ml_part), p.splits, Dv, n_rows, p.out, lse);
+  if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "mla_merge_kernel launch failed: %s", cudaGetErrorString(e));
+  return DSA_OK;
 }
 
 bool g_smem_big = false, g_smem_tiny = false;
@@ -787,9 +905,7 @@ extern "C" dsa_status_t sparse_mla_decode(const void* q, const void* kv_cache, i
   }
   st = launch_mla(p, q, kv_cache, Dk, Dv, s);
   if (st != DSA_OK || splits == 1) return st;
-  mla_merge_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, s>>>(p.o_part, p.ml_part, splits, Dv,
-                                                                                    p.out, lse);
-  return check_launch("mla_merge_kernel");
+  return launch_merge(p, Dv, lse, s);
 }
 
 extern "C" dsa_status_t sparse_mla_prefill(const void* q, const void* kv_cache, int64_t kv_block_stride,

@@ -54,11 +54,12 @@ def test_decode_b8_l131072_splits_agree():
         torch.cuda.synchronize()
         outs[s] = step.out.float().cpu().numpy()
     # the split count changes the summation order and the running maximum the
-    # bf16 softmax weights are taken against: a few bf16 ulp, far inside the
-    # attention tolerance
+    # bf16 softmax weights are taken against, so results differ by bf16
+    # rounding; a lost or doubled split would move outputs by far more than
+    # these bounds (a twentieth of the oracle's mean tolerance)
     for s in (8, 32):
         diff = np.abs(outs[s] - outs[1])
-        assert diff.max() <= 2e-3 and diff.mean() <= 2e-5, f"splits {s} vs 1: max {diff.max()} mean {diff.mean()}"
+        assert diff.max() <= 2e-3 and diff.mean() <= 1e-4, f"splits {s} vs 1: max {diff.max()} mean {diff.mean()}"
     for s in (1, 32):
         step.splits = s
         step.attention()
