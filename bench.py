@@ -242,12 +242,27 @@ def main():
         torch.cuda.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    # the timed steps: events only at step boundaries, so that nothing sits
+    # between the step's kernels (each is launched as a programmatic
+    # dependent of the one before)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     barrier()
     wall0 = time.perf_counter()
     for k in range(K):
         flush_l2()  # between steps: L2 holds nothing of the inputs, and nothing dirty
-        e = ev[k]
+        ev[k][0].record(stream)
+        step.run()
+        ev[k][1].record(stream)
+    barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    t_step = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    # per-kernel breakdown from separate steps with events between the kernels
+    Kb = max(5, min(K, 50))
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Kb)]
+    for k in range(Kb):
+        flush_l2()
+        e = evb[k]
         e[0].record(stream)
         step.indexer()
         e[1].record(stream)
@@ -256,12 +271,9 @@ def main():
         step.attention()
         e[3].record(stream)
     barrier()
-    wall = time.perf_counter() - wall0
-    clocks = sampler.stop()
-    t_step = [ev[k][0].elapsed_time(ev[k][3]) for k in range(K)]
-    t_idx = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
-    t_topk = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
-    t_att = [ev[k][2].elapsed_time(ev[k][3]) for k in range(K)]
+    t_idx = [evb[k][0].elapsed_time(evb[k][1]) for k in range(Kb)]
+    t_topk = [evb[k][1].elapsed_time(evb[k][2]) for k in range(Kb)]
+    t_att = [evb[k][2].elapsed_time(evb[k][3]) for k in range(Kb)]
     from deepseek_sparse_attention_fp8_gb300.replicas import aggregate
 
     ms, _, value = aggregate(float(np.mean(t_step)), wl.T, step.device)

@@ -35,6 +35,10 @@ dsa_status_t allow_smem(K kernel, int bytes, bool& done) {
   if (done) return DSA_OK;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "cudaFuncSetAttribute(%d bytes): %s", bytes, cudaGetErrorString(e));
+  // every kernel of the library asks for the same (largest) shared-memory
+  // carveout, so consecutive launches never wait for the SMs to be re-split
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "cudaFuncSetAttribute(carveout): %s", cudaGetErrorString(e));
   done = true;
   return DSA_OK;
 }

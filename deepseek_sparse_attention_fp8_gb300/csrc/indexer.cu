@@ -139,6 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the top-k kernel may be scheduled now; it waits for this grid's results
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = blockIdx.y / p.n_tb;
   const int tblk = blockIdx.y % p.n_tb;
   const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1);

@@ -150,17 +150,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   const int t = blockIdx.x / (kSplitDv * p.splits);
   const int kb0 = r == 0 ? 0 : C::kNkb0;          // first K-block (64 dims) this CTA owns
   const int nkb = r == 0 ? C::kNkb0 : C::kNkb1;   // K-blocks this CTA owns
-  const int b = find_request(p.qsl, p.B, t);
-  const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1);
-  int64_t valid64 = static_cast<int64_t>(__ldg(p.seq_lens + b)) - (q1 - q0) + (t - q0) + 1;
-  const int64_t cap = static_cast<int64_t>(p.bt_stride) * p.block_size;
-  if (valid64 > cap || valid64 < 1) {
-    if (tid == 0 && r == 0 && j == 0) report(p.dev_status, DSA_DEVERR_SEQ_LEN);
-    valid64 = max(static_cast<int64_t>(0), min(valid64, cap));
-  }
-  const int valid = static_cast<int>(valid64);
-  const int slot0 = j * p.per_split;
-  const int n_slots = max(0, min(p.K, slot0 + p.per_split) - slot0);
 
   uint8_t* kv_sm = smem + L::kKv;
   uint8_t* p_sm = smem + L::kP;
@@ -168,17 +157,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   int* row_sm = reinterpret_cast<int*>(smem + L::kRow);
   uint16_t* live_m = reinterpret_cast<uint16_t*>(smem + L::kLive);  // [stage][producer warp]: live-key bits
   int* coord_sm = reinterpret_cast<int*>(smem + L::kCoord);
-
-  // the softmax warps load their top-k slots before anything else
-  const int32_t* idx_row = p.topk + static_cast<int64_t>(t) * p.K + slot0;
-  int idx[8];
-  if (warp < 8) {
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int sl = u * 256 + tid;
-      idx[u] = sl < n_slots ? __ldg(idx_row + sl) : -1;
-    }
-  }
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -217,6 +195,31 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   }
   tc_fence_after();
   const uint32_t tmem = tmem_holder;
+
+  // Launched as a programmatic dependent: everything above touches no global
+  // memory; from here on the previous kernel's results are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = find_request(p.qsl, p.B, t);
+  const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1);
+  int64_t valid64 = static_cast<int64_t>(__ldg(p.seq_lens + b)) - (q1 - q0) + (t - q0) + 1;
+  const int64_t cap = static_cast<int64_t>(p.bt_stride) * p.block_size;
+  if (valid64 > cap || valid64 < 1) {
+    if (tid == 0 && r == 0 && j == 0) report(p.dev_status, DSA_DEVERR_SEQ_LEN);
+    valid64 = max(static_cast<int64_t>(0), min(valid64, cap));
+  }
+  const int valid = static_cast<int>(valid64);
+  const int slot0 = j * p.per_split;
+  const int n_slots = max(0, min(p.K, slot0 + p.per_split) - slot0);
+  // the softmax warps load their top-k slots first
+  const int32_t* idx_row = p.topk + static_cast<int64_t>(t) * p.K + slot0;
+  int idx[8];
+  if (warp < 8) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int sl = u * 256 + tid;
+      idx[u] = sl < n_slots ? __ldg(idx_row + sl) : -1;
+    }
+  }
 
   auto abort_now = [&](void) {
     s_abort = 1;
@@ -710,7 +713,11 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const float* __restrict_
   if (v == 0 && lse != nullptr) lse[row] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
 }
 
+bool g_smem_merge = false;
+
 dsa_status_t launch_merge(const MlaParams& p, int Dv, float* lse, cudaStream_t s) {
+  dsa_status_t st = allow_smem(mla_merge_kernel, 0, g_smem_merge);
+  if (st != DSA_OK) return st;
   const int64_t n_rows = static_cast<int64_t>(p.T) * p.H;
   const int rows_per_block = 128 / (Dv / 8);
   cudaLaunchConfig_t cfg = {};
@@ -765,13 +772,15 @@ dsa_status_t launch_mla(const MlaParams& p, const void* q, const void* kv, int D
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = MlaSmem<576, 512>::kTotal;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel<576, 512>, p, qmap, kvmap);
     if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "sparse_mla_kernel launch failed: %s", cudaGetErrorString(e));
   } else {

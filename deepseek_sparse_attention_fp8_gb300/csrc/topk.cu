@@ -1,35 +1,64 @@
-// a2: exact per-row top-k by radix select.
+// a2: exact per-row top-k.
 //
 // Each fp32 logit maps to a 32-bit key whose unsigned order is the float
-// order (-0.0 is folded onto +0.0 first, so the two tie). Four 8-bit radix
-// passes find the exact key T of the k-th largest element and how many
-// elements equal to T are needed; a final pass compacts, in position order,
-// every element above T plus the first `need` elements equal to T. The
-// output is therefore the exact top-k set with ties resolved toward the lower
+// order (-0.0 is folded onto +0.0 first, so the two tie). The selection
+// finds the exact key T of the k-th largest element and how many elements
+// equal to T are needed; a final pass compacts, in position order, every
+// element above T plus the first `need` elements equal to T. The output is
+// therefore the exact top-k set with ties resolved toward the lower
 // position, listed in ascending position.
 //
-// Long rows use two exact stages: the top-k of every 8192-key chunk, then
-// the top-k of the concatenated candidates. Any element of the global top-k
-// is in its chunk's top-k, and the candidates stay in position order, so the
-// second stage sees the same ties in the same order (vLLM PR #38476 review
-// thread: the global top-k is recoverable from per-chunk top-k candidates).
+// A row is cut into P contiguous parts (P = 1..8), one CTA each, the P CTAs
+// of a row forming a thread-block cluster that combines its histograms and
+// counts through distributed shared memory:
+//   1. each CTA stages its part's keys in shared memory and finds the part's
+//      finite minimum and maximum; the cluster's range gives 2048 bins that
+//      are linear in the value (outside values clamp to the end bins);
+//   2. the cluster's histogram of those bins gives, from its suffix sums, the
+//      bin holding the k-th largest key. The binning is monotonic, so every
+//      element of a higher bin is larger than every element of a lower one;
+//   3. T is the exact rank selection among that bin's elements (tens, for
+//      logits of a smooth distribution, gathered into every CTA), whose
+//      positions and the parts' counts above the bin also give each part's
+//      output offset. A bin of more than 512 elements is refined instead by
+//      histograms over its key interval, each level shrinking the interval
+//      2048-fold, until it holds one key; the parts then exchange counts;
+//   4. an ordered compaction writes each part's selected positions.
+// (vLLM PR #38476 review thread: index_topk selection, one exact top-k per
+// query row.)
 #include <algorithm>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 1024;
+using namespace ptx;
+
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 8192;       // keys per first-stage CTA
-constexpr int kCacheCap = 32768;   // rows up to this many keys are staged in shared memory
+constexpr int kMaxParts = 8;     // CTAs per row (portable cluster size)
+constexpr int kSegCap = 32768;   // keys of one part staged in shared memory
+constexpr int kBins = 2048;      // histogram bins
+constexpr int kCandCap = kThreads;  // threshold-bin elements ranked directly (one per thread)
 
 struct TopkShared {
-  uint32_t hist[kWarps][256];
-  uint32_t total[256];
-  uint32_t scan[kWarps];
-  uint32_t sel_digit, sel_gt;
+  uint32_t hist[kBins];   // this CTA's histogram (read by the peers)
+  uint32_t ghist[kBins];  // the row's histogram (slices written by the owners)
+  uint32_t cand_key[kCandCap];  // the threshold bin's elements of the whole row
+  int32_t cand_pos[kCandCap];
+  uint32_t loc_key[kCandCap];   // ... of this part
+  int32_t loc_pos[kCandCap];
+  uint32_t part_above[kMaxParts];  // per part: elements in bins above the threshold bin
+  uint32_t part_kmin[kMaxParts], part_kmax[kMaxParts];
+  uint32_t part_gt[kMaxParts], part_eq[kMaxParts];
+  uint32_t push_base[kMaxParts];
+  uint32_t cand_n, loc_n;
+  uint64_t scan[kWarps];
+  float red_f[2][kWarps];
+  uint32_t red_u[3][kWarps];
+  uint32_t bsel, above, thr;
 };
 
 __device__ __forceinline__ uint32_t order_key(float v) {
@@ -37,178 +66,99 @@ __device__ __forceinline__ uint32_t order_key(float v) {
   b = (b == 0x80000000u) ? 0u : b;
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
+// float value of an order key (the inverse map; -0.0 comes back as +0.0)
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+// Monotonic bin of v: v <= u implies bin(v) <= bin(u). NaNs go to the end
+// bin on the side their order key puts them.
+__device__ __forceinline__ int lin_bin(float v, float lo, float inv_w) {
+  if (v != v) return (__float_as_uint(v) & 0x80000000u) ? 0 : kBins - 1;
+  const float x = __fmul_rn(__fsub_rn(v, lo), inv_w);
+  return static_cast<int>(fminf(fmaxf(x, 0.f), static_cast<float>(kBins - 1)));
+}
 
-// position of token t inside its request: (request index, valid length)
-__device__ __forceinline__ int valid_length(const int32_t* seq_lens, const int32_t* qsl, int B, int t, int64_t ld) {
-  int lo = 0, hi = B - 1;  // last request with qsl[b] <= t
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(qsl + mid) <= t) lo = mid; else hi = mid - 1;
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t atom_add_cluster_u32(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+
+// valid(t): the number of leading positions of row t that are ranked. Every
+// thread of the block calls it: the request of token t is the last b with
+// query_start_loc[b] <= t, counted over the block in one round of loads.
+__device__ int valid_length(const int32_t* seq_lens, const int32_t* qsl, int B, int t, int64_t ld) {
+  int cnt = 0;
+  for (int j0 = 0; j0 < B; j0 += kThreads) {
+    const int j = j0 + static_cast<int>(threadIdx.x);
+    cnt += __syncthreads_count(j < B && __ldg(qsl + j) <= t);
   }
-  const int q0 = __ldg(qsl + lo), q1 = __ldg(qsl + lo + 1);
-  const int64_t v = static_cast<int64_t>(__ldg(seq_lens + lo)) - (q1 - q0) + (t - q0) + 1;
+  const int b = max(0, cnt - 1);
+  const int q0 = __ldg(qsl + b), q1 = __ldg(qsl + b + 1);
+  const int64_t v = static_cast<int64_t>(__ldg(seq_lens + b)) - (q1 - q0) + (t - q0) + 1;
   return static_cast<int>(max(static_cast<int64_t>(0), min(v, ld)));
 }
 
-// Exclusive block scan of `v` (1024 threads); returns the prefix, sets `total`.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t& total, TopkShared& sh) {
+// Exclusive block scan of `v`; returns the prefix and sets `total`. Two
+// 32-bit counts can travel packed in one 64-bit value.
+__device__ __forceinline__ uint64_t block_exclusive_scan(uint64_t v, uint64_t& total, TopkShared& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = v;
+  uint64_t x = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, off);
+    const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, x, off);
     if (lane >= off) x += y;
   }
   if (lane == 31) sh.scan[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t s = sh.scan[lane];
+    uint64_t s = lane < kWarps ? sh.scan[lane] : 0ull;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, s, off);
+      const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, s, off);
       if (lane >= off) s += y;
     }
-    sh.scan[lane] = s;  // inclusive over warps
+    if (lane < kWarps) sh.scan[lane] = s;  // inclusive over warps
   }
   __syncthreads();
-  const uint32_t before_warp = warp > 0 ? sh.scan[warp - 1] : 0u;
+  const uint64_t before_warp = warp > 0 ? sh.scan[warp - 1] : 0ull;
   total = sh.scan[kWarps - 1];
-  const uint32_t r = before_warp + x - v;
+  const uint64_t r = before_warp + x - v;
   __syncthreads();  // sh.scan is reused by the next call
   return r;
 }
 
-// Selects the k largest of n values (position i holds vals[i]; ids[i] < 0
-// marks an empty candidate). Writes min(k, n) results in position order to
-// out_idx (ids[i], or base + i when ids is null) and out_val (if non-null),
-// then pads up to k with -1 / -inf.
-__device__ void block_select(const float* __restrict__ vals, const int32_t* __restrict__ ids, int n, int k,
-                             int32_t base, int32_t* __restrict__ out_idx, float* __restrict__ out_val,
-                             uint32_t* kcache, TopkShared& sh) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  auto make_key = [&](int i) -> uint32_t {
-    if (ids != nullptr && __ldg(ids + i) < 0) return 0u;
-    return order_key(__ldg(vals + i));
-  };
-  auto emit = [&](int i, int pos) {
-    out_idx[pos] = ids != nullptr ? __ldg(ids + i) : base + i;
-    if (out_val != nullptr) out_val[pos] = __ldg(vals + i);
-  };
-  if (n <= k) {
-    for (int i = tid; i < n; i += kThreads) emit(i, i);
-    for (int i = n + tid; i < k; i += kThreads) {
-      out_idx[i] = -1;
-      if (out_val != nullptr) out_val[i] = -INFINITY;
-    }
-    return;
-  }
-  if (kcache != nullptr) {
-    // eight independent loads per thread in flight at a time
-    for (int base = 0; base < n; base += 8 * kThreads) {
-      uint32_t kk[8];
+// The bin of the row histogram `ghist` holding the `need`-th largest element
+// (bins scanned from the top): sets sh.bsel and sh.above (elements in higher
+// bins). Requires 1 <= need <= the histogram's total.
+__device__ void find_bin(TopkShared& sh, uint32_t need) {
+  const int tid = threadIdx.x;
+  constexpr int kPer = kBins / kThreads;  // bins per thread, descending
+  uint32_t h[kPer], sum = 0;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = base + u * kThreads + tid;
-        kk[u] = i < n ? make_key(i) : 0u;
-      }
+  for (int u = 0; u < kPer; ++u) {
+    h[u] = sh.ghist[kBins - 1 - (kPer * tid + u)];
+    sum += h[u];
+  }
+  uint64_t tot;
+  uint32_t before = static_cast<uint32_t>(block_exclusive_scan(sum, tot, sh));
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = base + u * kThreads + tid;
-        if (i < n) kcache[i] = kk[u];
-      }
+  for (int u = 0; u < kPer; ++u) {
+    if (before < need && need <= before + h[u]) {
+      sh.bsel = kBins - 1 - (kPer * tid + u);
+      sh.above = before;
     }
-    __syncthreads();
+    before += h[u];
   }
-  auto key_at = [&](int i) -> uint32_t { return kcache != nullptr ? kcache[i] : make_key(i); };
-
-  uint32_t prefix = 0, mask = 0;
-  int need = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < kWarps * 256; i += kThreads) (&sh.hist[0][0])[i] = 0u;
-    __syncthreads();
-    for (int i = tid; i < n; i += kThreads) {
-      const uint32_t key = key_at(i);
-      if ((key & mask) == prefix) atomicAdd(&sh.hist[warp][(key >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    uint32_t suffix = 0;  // elements whose digit is >= tid, within this warp's 32 digits
-    if (tid < 256) {
-      uint32_t s = 0;
-#pragma unroll 8
-      for (int w = 0; w < kWarps; ++w) s += sh.hist[w][tid];
-      sh.total[tid] = s;
-      suffix = s;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, suffix, off);
-        if (lane + off < 32) suffix += y;
-      }
-      if (lane == 0) sh.scan[warp] = suffix;
-    }
-    __syncthreads();
-    if (tid < 256) {
-      uint32_t above = 0;  // elements in digits of higher warps
-      for (int w = warp + 1; w < 8; ++w) above += sh.scan[w];
-      const uint32_t incl = suffix + above;  // elements with digit >= tid
-      const uint32_t gt = incl - sh.total[tid];        // elements with digit > tid
-      if (gt < static_cast<uint32_t>(need) && static_cast<uint32_t>(need) <= incl) {
-        sh.sel_digit = tid;
-        sh.sel_gt = gt;
-      }
-    }
-    __syncthreads();
-    need -= static_cast<int>(sh.sel_gt);
-    prefix |= sh.sel_digit << shift;
-    mask |= 255u << shift;
-    __syncthreads();
-  }
-  const uint32_t thr = prefix;
-
-  // ordered compaction: everything above thr, then the first `need` equal to thr
-  if (kcache != nullptr) {
-    // staged rows: each thread owns one contiguous segment, one block scan
-    const int seg = (n + kThreads - 1) / kThreads;
-    const int lo = min(n, tid * seg), hi = min(n, lo + seg);
-    uint32_t cg = 0, ce = 0;
-    for (int i = lo; i < hi; ++i) {
-      const uint32_t key = kcache[i];
-      cg += key > thr;
-      ce += key == thr;
-    }
-    uint32_t total;
-    const uint32_t before = block_exclusive_scan(cg | (ce << 16), total, sh);
-    uint32_t g = before & 0xFFFFu, e = before >> 16;
-    for (int i = lo; i < hi; ++i) {
-      const uint32_t key = kcache[i];
-      if (key > thr) {
-        emit(i, static_cast<int>(g + min(e, static_cast<uint32_t>(need))));
-        ++g;
-      } else if (key == thr) {
-        if (e < static_cast<uint32_t>(need)) emit(i, static_cast<int>(g + e));
-        ++e;
-      }
-    }
-    return;
-  }
-  uint32_t run_gt = 0, run_eq = 0;
-  for (int start = 0; start < n; start += kThreads) {
-    const int i = start + tid;
-    uint32_t key = 0;
-    bool gt = false, eq = false;
-    if (i < n) {
-      key = key_at(i);
-      gt = key > thr;
-      eq = key == thr;
-    }
-    uint32_t total;
-    const uint32_t before = block_exclusive_scan((gt ? 1u : 0u) | (eq ? 0x10000u : 0u), total, sh);
-    const uint32_t gt_before = run_gt + (before & 0xFFFFu);
-    const uint32_t eq_before = run_eq + (before >> 16);
-    if (gt) emit(i, static_cast<int>(gt_before + min(eq_before, static_cast<uint32_t>(need))));
-    if (eq && eq_before < static_cast<uint32_t>(need)) emit(i, static_cast<int>(gt_before + eq_before));
-    run_gt += total & 0xFFFFu;
-    run_eq += total >> 16;
-  }
+  __syncthreads();
 }
 
 struct TopkParams {
@@ -216,55 +166,288 @@ struct TopkParams {
   int64_t ld;
   const int32_t* seq_lens;
   const int32_t* qsl;
-  int B, k, nchunks;
+  int B, k, parts;
   int32_t* out;
-  int32_t* cand_idx;
-  float* cand_val;
-  int use_cache;
 };
 
-__global__ void __launch_bounds__(kThreads) topk_single_kernel(const TopkParams p) {
-  extern __shared__ uint32_t kcache[];
+// kCached: the part's keys are staged in shared memory (else re-read)
+template <bool kCached>
+__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
+  extern __shared__ uint32_t kc[];  // this part's keys (when cached)
   __shared__ TopkShared sh;
-  const int t = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // launched as a programmatic dependent of the logits producer: wait for
+  // its results, then let the next kernel's CTAs be scheduled
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int P = p.parts;
+  const int r = static_cast<int>(cluster_ctarank());
+  const int t = blockIdx.x / P;
   const int n = valid_length(p.seq_lens, p.qsl, p.B, t, p.ld);
-  block_select(p.logits + static_cast<int64_t>(t) * p.ld, nullptr, n, p.k, 0, p.out + static_cast<int64_t>(t) * p.k,
-               nullptr, (p.use_cache && n <= kCacheCap) ? kcache : nullptr, sh);
-}
-
-__global__ void __launch_bounds__(kThreads) topk_stage1_kernel(const TopkParams p) {
-  extern __shared__ uint32_t kcache[];
-  __shared__ TopkShared sh;
-  const int c = blockIdx.x, t = blockIdx.y;
-  const int valid = valid_length(p.seq_lens, p.qsl, p.B, t, p.ld);
-  if (valid <= p.k) return;  // the second stage writes such rows directly
-  const int begin = c * kChunk;
-  const int n = max(0, min(valid - begin, kChunk));
-  const int64_t slot = (static_cast<int64_t>(t) * p.nchunks + c) * p.k;
-  block_select(p.logits + static_cast<int64_t>(t) * p.ld + begin, nullptr, n, p.k, begin, p.cand_idx + slot,
-               p.cand_val + slot, kcache, sh);
-}
-
-__global__ void __launch_bounds__(kThreads) topk_stage2_kernel(const TopkParams p) {
-  extern __shared__ uint32_t kcache[];
-  __shared__ TopkShared sh;
-  const int t = blockIdx.x;
-  const int valid = valid_length(p.seq_lens, p.qsl, p.B, t, p.ld);
-  int32_t* out = p.out + static_cast<int64_t>(t) * p.k;
-  if (valid <= p.k) {
-    block_select(p.logits + static_cast<int64_t>(t) * p.ld, nullptr, valid, p.k, 0, out, nullptr, nullptr, sh);
+  const int k = p.k;
+  int32_t* out = p.out + static_cast<int64_t>(t) * k;
+  if (n <= k) {  // every valid position, then -1 (the same branch for the whole cluster)
+    const int o0 = static_cast<int>(static_cast<int64_t>(r) * k / P);
+    const int o1 = static_cast<int>(static_cast<int64_t>(r + 1) * k / P);
+    for (int i = o0 + tid; i < o1; i += kThreads) out[i] = i < n ? i : -1;
     return;
   }
-  const int n = p.nchunks * p.k;
-  const int64_t slot = static_cast<int64_t>(t) * n;
-  block_select(p.cand_val + slot, p.cand_idx + slot, n, p.k, 0, out, nullptr, (p.use_cache && n <= kCacheCap) ? kcache : nullptr,
-               sh);
+  const float* row = p.logits + static_cast<int64_t>(t) * p.ld;
+  const int seg = (n + P - 1) / P;
+  const int s0 = min(n, r * seg);
+  const int m = min(n, s0 + seg) - s0;  // this part's length (may be 0)
+  auto key_at = [&](int i) -> uint32_t {
+    if constexpr (kCached) return kc[i];
+    else return order_key(__ldg(row + s0 + i));
+  };
+  auto remote = [&](const void* ptr, int q) -> uint32_t { return mapa_shared(smem_u32(ptr), static_cast<uint32_t>(q)); };
+
+  // ---- 1. bin range: the finite min and max of 1024 evenly spaced samples of
+  // the row, the same in every CTA of the row
+  for (int b = tid; b < kBins; b += kThreads) sh.hist[b] = 0u;
+  if (tid == 0) {
+    sh.cand_n = 0u;
+    sh.loc_n = 0u;
+  }
+  float lo = INFINITY, hi = -INFINITY;
+  {
+    const int ns = min(n, 1024);
+#pragma unroll
+    for (int u = 0; u < 1024 / kThreads; ++u) {
+      const int j = u * kThreads + tid;
+      if (j < ns) {
+        const float v = __ldg(row + static_cast<int64_t>(j) * n / ns);
+        if (isfinite(v)) {
+          lo = fminf(lo, v);
+          hi = fmaxf(hi, v);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
+      hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, off));
+    }
+    if (lane == 0) {
+      sh.red_f[0][warp] = lo;
+      sh.red_f[1][warp] = hi;
+    }
+    __syncthreads();
+    lo = INFINITY;
+    hi = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      lo = fminf(lo, sh.red_f[0][w]);
+      hi = fmaxf(hi, sh.red_f[1][w]);
+    }
+  }
+  float inv_w = hi > lo ? static_cast<float>(kBins) / (hi - lo) : 0.f;
+  if (!isfinite(inv_w)) inv_w = 0.f;
+  if (!(lo <= hi)) lo = 0.f;
+
+  // ---- 2. stage the keys and count them into the part's histogram; CTA r
+  // then sums its slice of bins over the cluster and writes the sums into
+  // every CTA
+  for (int base = 0; base < m; base += 8 * kThreads) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = base + u * kThreads + tid;
+      v[u] = i < m ? __ldg(row + s0 + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = base + u * kThreads + tid;
+      if (i < m) {
+        const uint32_t key = order_key(v[u]);
+        if constexpr (kCached) kc[i] = key;
+        atomicAdd(&sh.hist[lin_bin(key_value(key), lo, inv_w)], 1u);
+      }
+    }
+  }
+  const int sl0 = r * (kBins / P), sl1 = (r + 1) * (kBins / P);
+  auto reduce_hist = [&]() {
+    cluster_sync_all();  // every local histogram is complete
+    for (int b = sl0 + tid; b < sl1; b += kThreads) {
+      uint32_t s = 0;
+      for (int q = 0; q < P; ++q) s += ld_cluster_u32(remote(&sh.hist[b], q));
+      for (int q = 0; q < P; ++q) st_cluster_u32(remote(&sh.ghist[b], q), s);
+    }
+    cluster_sync_all();  // every CTA holds the whole row histogram
+  };
+  reduce_hist();
+  find_bin(sh, static_cast<uint32_t>(k));
+  const int bsel = static_cast<int>(sh.bsel);
+  const uint32_t c = sh.ghist[bsel];
+  const bool direct = c <= static_cast<uint32_t>(kCandCap);  // the same in every CTA
+  int need = k - static_cast<int>(sh.above);  // elements still to take from the bin: 1..c
+
+  // ---- 3. the part's elements of the threshold bin go to every CTA, with
+  // the part's count above that bin and its key range within it
+  {
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u, above = 0u;
+    for (int i0 = 0; i0 < m; i0 += 4 * kThreads) {
+      uint32_t kk[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        kk[u] = i < m ? key_at(i) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        if (i >= m) continue;
+        const int b = lin_bin(key_value(kk[u]), lo, inv_w);
+        above += b > bsel;
+        if (b != bsel) continue;
+        kmin = min(kmin, kk[u]);
+        kmax = max(kmax, kk[u]);
+        if (direct) {
+          const uint32_t slot = atomicAdd(&sh.loc_n, 1u);
+          sh.loc_key[slot] = kk[u];
+          sh.loc_pos[slot] = s0 + i;
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, off));
+      kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, off));
+      above += __shfl_xor_sync(0xFFFFFFFFu, above, off);
+    }
+    if (lane == 0) {
+      sh.red_u[0][warp] = kmin;
+      sh.red_u[1][warp] = kmax;
+      sh.red_u[2][warp] = above;
+    }
+    __syncthreads();
+    const uint32_t ln = sh.loc_n;
+    if (tid < P) {
+      uint32_t a = 0xFFFFFFFFu, b = 0u, ab = 0u;
+      for (int w = 0; w < kWarps; ++w) {
+        a = min(a, sh.red_u[0][w]);
+        b = max(b, sh.red_u[1][w]);
+        ab += sh.red_u[2][w];
+      }
+      st_cluster_u32(remote(&sh.part_kmin[r], tid), a);
+      st_cluster_u32(remote(&sh.part_kmax[r], tid), b);
+      st_cluster_u32(remote(&sh.part_above[r], tid), ab);
+      if (direct) sh.push_base[tid] = atom_add_cluster_u32(remote(&sh.cand_n, tid), ln);  // slots in CTA tid
+    }
+    __syncthreads();
+    if (direct) {
+      for (int e = tid; e < static_cast<int>(ln) * P; e += kThreads) {
+        const int q = e / static_cast<int>(ln), j = e - q * static_cast<int>(ln);
+        const uint32_t slot = sh.push_base[q] + j;
+        st_cluster_u32(remote(&sh.cand_key[slot], q), sh.loc_key[j]);
+        st_cluster_u32(remote(&sh.cand_pos[slot], q), static_cast<uint32_t>(sh.loc_pos[j]));
+      }
+    }
+    cluster_sync_all();  // after this, no CTA reads or writes another's shared memory
+                         // unless the bin is refined below
+  }
+
+  // ---- 4. the threshold key T and, per part, the output offsets
+  uint32_t thr;
+  uint32_t g_base = 0, e_base = 0;  // elements > T and == T in the parts before this one
+  if (direct) {
+    // rank of each candidate: larger key first, then lower position
+    if (tid < static_cast<int>(c)) {
+      const uint32_t key = sh.cand_key[tid];
+      const int pos = sh.cand_pos[tid];
+      int rank = 0;
+      for (int j = 0; j < static_cast<int>(c); ++j) {
+        const uint32_t kj = sh.cand_key[j];
+        rank += (kj > key) || (kj == key && sh.cand_pos[j] < pos);
+      }
+      if (rank == need - 1) sh.thr = key;
+    }
+    __syncthreads();
+    thr = sh.thr;
+    const bool mine = tid < static_cast<int>(c);
+    need -= __syncthreads_count(mine && sh.cand_key[tid] > thr);
+    for (int q = 0; q < r; ++q) g_base += sh.part_above[q];
+    g_base += __syncthreads_count(mine && sh.cand_pos[tid] < s0 && sh.cand_key[tid] > thr);
+    e_base = __syncthreads_count(mine && sh.cand_pos[tid] < s0 && sh.cand_key[tid] == thr);
+  } else {
+    // refine over the bin's key interval [klo, khi] until it holds one key
+    uint32_t klo = 0xFFFFFFFFu, khi = 0u;
+    for (int q = 0; q < P; ++q) {
+      klo = min(klo, sh.part_kmin[q]);
+      khi = max(khi, sh.part_kmax[q]);
+    }
+    while (klo < khi) {  // the same trip count in every CTA of the row
+      const uint64_t R = static_cast<uint64_t>(khi - klo) + 1;
+      for (int b = tid; b < kBins; b += kThreads) sh.hist[b] = 0u;
+      __syncthreads();
+      for (int i = tid; i < m; i += kThreads) {
+        const uint32_t key = key_at(i);
+        if (key >= klo && key <= khi)
+          atomicAdd(&sh.hist[static_cast<int>((static_cast<uint64_t>(key - klo) * kBins) / R)], 1u);
+      }
+      reduce_hist();
+      find_bin(sh, static_cast<uint32_t>(need));
+      const uint64_t b = sh.bsel;
+      need -= static_cast<int>(sh.above);
+      const uint32_t nlo = klo + static_cast<uint32_t>((b * R + kBins - 1) / kBins);
+      const uint32_t nhi = klo + static_cast<uint32_t>(((b + 1) * R + kBins - 1) / kBins) - 1u;
+      klo = nlo;
+      khi = nhi;
+    }
+    thr = klo;
+  }
+
+  // ---- 5. ordered compaction: warp w takes a contiguous run of the part,
+  // 32 consecutive keys at a time; ballots give the order within a step
+  const int wrun = (((m + kWarps - 1) / kWarps) + 31) & ~31;
+  const int w0 = min(m, warp * wrun), w1 = min(m, w0 + wrun);
+  uint32_t cg = 0, ce = 0;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < w1 ? key_at(i) : 0u;
+    cg += __popc(__ballot_sync(0xFFFFFFFFu, i < w1 && key > thr));
+    ce += __popc(__ballot_sync(0xFFFFFFFFu, i < w1 && key == thr));
+  }
+  uint64_t tot;
+  const uint64_t wpre = block_exclusive_scan(lane == 0 ? (static_cast<uint64_t>(cg) | (static_cast<uint64_t>(ce) << 32)) : 0ull,
+                                             tot, sh);
+  const uint64_t wbefore = __shfl_sync(0xFFFFFFFFu, wpre, 0);
+  if (!direct) {  // the parts' counts give the offsets
+    if (tid < P) {
+      st_cluster_u32(remote(&sh.part_gt[r], tid), static_cast<uint32_t>(tot));
+      st_cluster_u32(remote(&sh.part_eq[r], tid), static_cast<uint32_t>(tot >> 32));
+    }
+    cluster_sync_all();  // no shared-memory access between the CTAs after this
+    for (int q = 0; q < r; ++q) {
+      g_base += sh.part_gt[q];
+      e_base += sh.part_eq[q];
+    }
+  }
+  uint32_t g = g_base + static_cast<uint32_t>(wbefore), e = e_base + static_cast<uint32_t>(wbefore >> 32);
+  const uint32_t nq = static_cast<uint32_t>(need);
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < w1 ? key_at(i) : 0u;
+    const bool gt = i < w1 && key > thr, eq = i < w1 && key == thr;
+    const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), be = __ballot_sync(0xFFFFFFFFu, eq);
+    const uint32_t gi = g + __popc(bg & lt), ei = e + __popc(be & lt);
+    if (gt) out[gi + min(ei, nq)] = s0 + i;
+    if (eq && ei < nq) out[gi + ei] = s0 + i;
+    g += __popc(bg);
+    e += __popc(be);
+  }
 }
 
-bool g_smem_single = false, g_smem_s1 = false, g_smem_s2 = false;
+bool g_smem = false, g_smem_u = false;
 
-bool use_two_stage(int32_t T, int64_t ld, int32_t k) {
-  return ld > 2 * kChunk && k < kChunk && T < 2 * num_sms();
+// CTAs per row: as many as fill the GPU once (at most 8), and enough that a
+// part fits the shared-memory stage where possible.
+int parts_for(int32_t T, int64_t ld) {
+  int P = 1;
+  while (P < kMaxParts && static_cast<int64_t>(T) * P * 2 <= num_sms() && (ld + 2 * P - 1) / (2 * P) >= 1024) P *= 2;
+  while (P < kMaxParts && (ld + P - 1) / P > kSegCap) P *= 2;
+  return P;
 }
 
 }  // namespace
@@ -273,24 +456,27 @@ bool use_two_stage(int32_t T, int64_t ld, int32_t k) {
 using namespace dsa;
 
 extern "C" size_t dsa_topk_workspace_size(int32_t T, int64_t ld, int32_t index_topk) {
-  if (T <= 0 || ld <= 0 || index_topk <= 0) return 0;
-  if (!use_two_stage(T, ld, index_topk)) return 0;
-  const int64_t nchunks = (ld + kChunk - 1) / kChunk;
-  return static_cast<size_t>(T) * nchunks * index_topk * (sizeof(int32_t) + sizeof(float));
+  (void)T;
+  (void)ld;
+  (void)index_topk;
+  return 0;  // the CTAs of a row combine their counts in distributed shared memory
 }
 
 extern "C" dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t* seq_lens,
                                  const int32_t* query_start_loc, int32_t B, int32_t T, int32_t index_topk,
                                  int32_t* topk_idx, void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+  (void)workspace;
+  (void)ws_bytes;
   if (B < 0 || T < 0 || ld <= 0 || index_topk <= 0)
     return fail(DSA_ERR_INVALID_ARG, "dsa_topk: bad sizes B=%d T=%d ld=%lld k=%d", B, T, (long long)ld, index_topk);
   if (T == 0) return DSA_OK;
   if (B == 0) return fail(DSA_ERR_INVALID_ARG, "dsa_topk: T > 0 with B == 0");
   if (!logits || !seq_lens || !query_start_loc || !topk_idx) return fail(DSA_ERR_INVALID_ARG, "dsa_topk: null pointer");
   if (index_topk > 65535) return fail(DSA_ERR_UNSUPPORTED, "dsa_topk: index_topk %d > 65535", index_topk);
+  if (ld > 0x7FFFFFFF) return fail(DSA_ERR_UNSUPPORTED, "dsa_topk: ld %lld does not fit int32 positions", (long long)ld);
+  if (static_cast<int64_t>(T) * kMaxParts > 0x7FFFFFFF) return fail(DSA_ERR_UNSUPPORTED, "dsa_topk: T too large");
   dsa_status_t st = check_device();
   if (st != DSA_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   TopkParams p;
   p.logits = logits;
   p.ld = ld;
@@ -299,35 +485,27 @@ extern "C" dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t*
   p.B = B;
   p.k = index_topk;
   p.out = topk_idx;
-  p.cand_idx = nullptr;
-  p.cand_val = nullptr;
-  p.nchunks = 0;
-  p.use_cache = 1;
-  if (use_two_stage(T, ld, index_topk)) {
-    const size_t need = dsa_topk_workspace_size(T, ld, index_topk);
-    if (workspace == nullptr || ws_bytes < need)
-      return fail(DSA_ERR_WORKSPACE, "dsa_topk: needs %zu workspace bytes, got %zu", need, ws_bytes);
-    p.nchunks = static_cast<int>((ld + kChunk - 1) / kChunk);
-    p.cand_idx = static_cast<int32_t*>(workspace);
-    p.cand_val = reinterpret_cast<float*>(p.cand_idx + static_cast<int64_t>(T) * p.nchunks * index_topk);
-    const int s1 = kChunk * 4;
-    st = allow_smem(topk_stage1_kernel, s1, g_smem_s1);
-    if (st != DSA_OK) return st;
-    topk_stage1_kernel<<<dim3(p.nchunks, T), kThreads, s1, s>>>(p);
-    st = check_launch("topk_stage1_kernel");
-    if (st != DSA_OK) return st;
-    const int n2 = p.nchunks * index_topk;
-    const int s2 = (n2 <= kCacheCap ? n2 : 0) * 4;
-    p.use_cache = n2 <= kCacheCap;
-    st = allow_smem(topk_stage2_kernel, kCacheCap * 4, g_smem_s2);
-    if (st != DSA_OK) return st;
-    topk_stage2_kernel<<<T, kThreads, s2, s>>>(p);
-    return check_launch("topk_stage2_kernel");
-  }
-  const int64_t cache_keys = ld <= kCacheCap ? ld : 0;
-  p.use_cache = cache_keys > 0;
-  st = allow_smem(topk_single_kernel, kCacheCap * 4, g_smem_single);
+  p.parts = parts_for(T, ld);
+  const int64_t seg = (ld + p.parts - 1) / p.parts;
+  const bool cached = seg <= kSegCap;
+  const int smem = cached ? static_cast<int>(seg * 4) : 0;
+  st = cached ? allow_smem(topk_kernel<true>, kSegCap * 4, g_smem) : allow_smem(topk_kernel<false>, 0, g_smem_u);
   if (st != DSA_OK) return st;
-  topk_single_kernel<<<T, kThreads, static_cast<int>(cache_keys * 4), s>>>(p);
-  return check_launch("topk_single_kernel");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(T) * p.parts));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.parts;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cached ? cudaLaunchKernelEx(&cfg, topk_kernel<true>, p) : cudaLaunchKernelEx(&cfg, topk_kernel<false>, p);
+  if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "topk_kernel launch failed: %s", cudaGetErrorString(e));
+  return DSA_OK;
 }

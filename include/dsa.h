@@ -123,10 +123,11 @@ dsa_status_t dsa_indexer_logits(const void* q_idx, int64_t q_stride_t, const flo
  * +0.0); the n = min(index_topk, valid(t)) largest are selected, equal values
  * resolved toward the lower position. topk_idx [T, index_topk] receives the n
  * selected positions in ascending position order, then -1 in the remaining
- * slots. Rows longer than the single-pass limit are selected in two exact
- * stages (per-chunk top-k, then top-k of the candidates), which needs
- * `workspace` of dsa_topk_workspace_size() bytes (may be NULL when that is 0).
- * (vLLM PR #38476 review thread: index_topk selection; chunked exact top-k.)
+ * slots. A row is shared by up to 8 CTAs of one cluster, which combine their
+ * histograms in distributed shared memory: dsa_topk_workspace_size() is 0 and
+ * `workspace` may be NULL (both stay in the interface for callers that size a
+ * workspace generically). Requires ld < 2^31 and index_topk <= 65535.
+ * (vLLM PR #38476 review thread: index_topk selection.)
  */
 size_t dsa_topk_workspace_size(int32_t T, int64_t ld, int32_t index_topk);
 dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* query_start_loc,

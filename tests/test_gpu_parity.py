@@ -94,14 +94,48 @@ def test_topk_ties_and_signed_zero():
     check_topk_sets(got, ref, range(T))
 
 
+@pytest.mark.parametrize("T,ld,K,dist", [(5, 8192, 2048, "normal"), (4, 32768, 2048, "normal"),
+                                         (304, 36000, 2048, "normal"), (4, 8192, 100, "normal"),
+                                         (4, 8192, 2048, "outliers"), (4, 8192, 2048, "constant_bins"),
+                                         (2, 32768, 2048, "ties_across_parts")])
+def test_topk_histogram_paths(T, ld, K, dist):
+    """Logits of a smooth distribution (the threshold bin holds few keys), rows
+    staged in shared memory and rows read from global memory (T >= 2 x SMs),
+    a small k; two cases that force the refinement of the threshold bin:
+    +-1e30 outliers inside the sampled range (one bin holds almost
+    everything) and values of a few distinct levels; and equal values spread
+    over all the CTAs of a row, ranked by position in the direct path."""
+    rng = np.random.default_rng(T * 7 + ld + K)
+    vals = rng.standard_normal((T, ld)).astype(np.float32)
+    if dist == "outliers":
+        vals[:, 0] = 1e30
+        vals[:, 8] = -1e30
+        vals[:, 16] = np.inf
+    elif dist == "constant_bins":
+        vals = np.round(vals * 2).astype(np.float32)
+    elif dist == "ties_across_parts":  # ~80 copies of each of 400 levels, spread over the whole row
+        vals = rng.integers(-200, 200, (T, ld)).astype(np.float32)
+    seq = np.full(T, ld, np.int32)
+    seq[-1] = ld - 777
+    qsl = np.arange(T + 1, dtype=np.int32)
+    got = api.dsa_topk(torch.from_numpy(vals).cuda(), torch.from_numpy(seq).cuda(), torch.from_numpy(qsl).cuda(),
+                       K).cpu().numpy()
+    ref = O.topk(vals, seq, qsl, K)
+    check_topk_sets(got, ref, range(T))
+    for t in range(T):
+        g = got[t][got[t] >= 0]
+        assert np.all(np.diff(g) > 0)
+
+
 @pytest.mark.parametrize("ld", [40000, 131072])
-def test_topk_two_stage_matches_full_sort(ld):
+def test_topk_long_rows_match_full_sort(ld):
+    """Long rows shared by a cluster of CTAs, integer-valued (heavy ties
+    across the CTAs of a row)."""
     T, K = 3, 2048
     rng = np.random.default_rng(ld)
     vals = rng.integers(-50, 50, (T, ld)).astype(np.float32)
     seq = np.array([ld, ld - 12345, 3000], np.int32)
     qsl = np.arange(T + 1, dtype=np.int32)
-    assert api.dsa_topk_workspace_size(T, ld, K) > 0
     got = api.dsa_topk(torch.from_numpy(vals).cuda(), torch.from_numpy(seq).cuda(), torch.from_numpy(qsl).cuda(),
                        K).cpu().numpy()
     ref = O.topk(vals, seq, qsl, K)

@@ -62,9 +62,9 @@ def test_topk_rejects_bad_arguments(api):
 
 
 def test_workspace_sizes(api):
-    assert api.dsa_topk_workspace_size(32, 8192, 2048) == 0  # single pass
-    ws = api.dsa_topk_workspace_size(8, 131072, 2048)
-    assert ws == 8 * 16 * 2048 * 8
+    # the CTAs of a row combine their histograms in distributed shared memory
+    for T, ld in ((32, 8192), (8, 131072), (4096, 65536), (1, 1 << 20)):
+        assert api.dsa_topk_workspace_size(T, ld, 2048) == 0
     assert api.sparse_mla_workspace_size(32, 128, 512, 1) == 0
     assert api.sparse_mla_workspace_size(8, 128, 512, 8) == 8 * 128 * 8 * (512 * 4 + 8)
 
