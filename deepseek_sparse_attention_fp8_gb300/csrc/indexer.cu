@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
                                                                      const __grid_constant__ CUtensorMap kmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], acc_full[2], acc_empty[2];
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], acc_full[2], acc_empty[2], q_ready;
   __shared__ uint32_t tmem_holder;
   __shared__ int s_tok[kMaxTokensPerCta];
   __shared__ int s_valid[kMaxTokensPerCta];
@@ -184,42 +184,33 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
   uint32_t tmem = 0;
   const uint32_t acc_cols = n_cols <= 32 ? 32 : (n_cols <= 64 ? 64 : (n_cols <= 128 ? 128 : 256));
   const uint32_t tmem_cols = acc_cols * nbuf;
+  // ---- prologue. The key loads start as soon as the block ids are known;
+  // warps 0-3 quantise the queries meanwhile (the MMA waits on q_ready).
+  // a0 takes 16 (token, head) rows per pass, 8 lanes per row; the loads of
+  // every pass are issued before the barrier so their latency overlaps it.
+  constexpr int kQPass = 4;  // passes in flight: 64 rows (up to 4 tokens x 16 heads, or 1 token x 64 heads)
+  uint4 qa[kQPass], qb[kQPass];
+  float qw[kQPass];
   if (n_comp > 0) {
     if constexpr (DI < 128) {  // row padding past Di is never written by the loads
       for (int i = tid; i < S * kTileBytes / 16; i += kThreads) reinterpret_cast<uint4*>(sk)[i] = make_uint4(0, 0, 0, 0);
     }
     if (warp < 4) {
-      // a0: quantise the token block's queries into the B operand (N rows x 128 B).
-      // 16 rows per pass (8 lanes per row); the loads of up to 4 passes are
-      // issued together so their latencies overlap.
-      for (int base0 = 0; base0 < n_cols; base0 += 4 * 16) {
-        uint4 a[4], bq[4];
-        float wv[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int n = base0 + u * 16 + tid / 8, c = tid % 8;
-          const int j = n / p.hi_pad, h = n % p.hi_pad;
-          a[u] = make_uint4(0, 0, 0, 0);
-          bq[u] = a[u];
-          wv[u] = 0.f;
-          if (n < n_cols && j < ntok && h < p.Hi) {
-            if (c < DI / 16) {
-              const uint4* src =
-                  reinterpret_cast<const uint4*>(p.q + (tok0 + j) * p.q_stride_t + static_cast<int64_t>(h) * DI) + 2 * c;
-              a[u] = __ldg(src);
-              bq[u] = __ldg(src + 1);
-            }
-            if (c == 0) wv[u] = __ldg(p.w + static_cast<int64_t>(tok0 + j) * p.Hi + h);
+      for (int u = 0; u < kQPass; ++u) {
+        const int n = u * 16 + tid / 8, c = tid % 8;
+        const int j = n / p.hi_pad, h = n % p.hi_pad;
+        qa[u] = make_uint4(0, 0, 0, 0);
+        qb[u] = qa[u];
+        qw[u] = 0.f;
+        if (n < n_cols && j < ntok && h < p.Hi) {
+          if (c < DI / 16) {
+            const uint4* src =
+                reinterpret_cast<const uint4*>(p.q + (tok0 + j) * p.q_stride_t + static_cast<int64_t>(h) * DI) + 2 * c;
+            qa[u] = __ldg(src);
+            qb[u] = __ldg(src + 1);
           }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int n = base0 + u * 16 + tid / 8, c = tid % 8;
-          if (base0 + u * 16 >= n_cols) break;  // uniform across the block
-          float scale;
-          const uint4 codes = quant_chunk16(a[u], bq[u], scale);
-          *reinterpret_cast<uint4*>(sq + sw128_offset(n, c)) = codes;
-          if (c == 0) sw[n] = wv[u] * scale;  // zero for padded rows
+          if (c == 0) qw[u] = __ldg(p.w + static_cast<int64_t>(tok0 + j) * p.Hi + h);
         }
       }
     } else {
@@ -229,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
         s_blk[i] = lb * p.block_size < seq_len ? __ldg(bt_row + lb) : -1;
       }
     }
-    fence_proxy_async_smem();
+    if (DI < 128) fence_proxy_async_smem();
     if (warp == 5) {
       tmem_alloc(&tmem_holder, tmem_cols);
       tmem_relinquish();
@@ -243,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
         mbar_init(&acc_full[s], 1);
         mbar_init(&acc_empty[s], 4);
       }
+      mbar_init(&q_ready, 4);
       fence_mbar_init();
     }
   }
@@ -250,6 +242,44 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   if (n_comp > 0) tmem = tmem_holder;
+  if (n_comp > 0 && warp < 4) {
+    // a0: the token block's queries -> the B operand (N rows x 128 B) and
+    // the per-column weight w * scale_q
+    for (int base0 = 0; base0 < n_cols; base0 += kQPass * 16) {
+      if (base0 > 0) {  // more than 64 columns: the later passes load here
+#pragma unroll
+        for (int u = 0; u < kQPass; ++u) {
+          const int n = base0 + u * 16 + tid / 8, c = tid % 8;
+          const int j = n / p.hi_pad, h = n % p.hi_pad;
+          qa[u] = make_uint4(0, 0, 0, 0);
+          qb[u] = qa[u];
+          qw[u] = 0.f;
+          if (n < n_cols && j < ntok && h < p.Hi) {
+            if (c < DI / 16) {
+              const uint4* src =
+                  reinterpret_cast<const uint4*>(p.q + (tok0 + j) * p.q_stride_t + static_cast<int64_t>(h) * DI) + 2 * c;
+              qa[u] = __ldg(src);
+              qb[u] = __ldg(src + 1);
+            }
+            if (c == 0) qw[u] = __ldg(p.w + static_cast<int64_t>(tok0 + j) * p.Hi + h);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kQPass; ++u) {
+        const int n = base0 + u * 16 + tid / 8, c = tid % 8;
+        if (base0 + u * 16 >= n_cols) break;  // uniform across the four warps
+        float scale;
+        const uint4 codes = quant_chunk16(qa[u], qb[u], scale);
+        *reinterpret_cast<uint4*>(sq + sw128_offset(n, c)) = codes;
+        if (c == 0) sw[n] = qw[u] * scale;  // zero for padded rows
+      }
+    }
+    fence_proxy_async_smem();  // the MMA reads the codes through the async proxy
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&q_ready);
+    named_barrier_sync(1, 128);  // every column weight is written before the epilogue reads them
+  }
 
   auto abort_now = [&](void) {
     s_abort = 1;
@@ -334,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
   } else if (n_comp > 0 && warp == 5) {
     // ---------------- MMA issuer
     const uint32_t idesc = idesc_e4m3(128, n_cols);
+    if (!mbar_wait(&q_ready, 0) && lane == 0) abort_now();
     for (int i = 0; i < n_comp && !s_abort; ++i) {
       const int st = i % S, buf = i % nbuf;
       bool ok = mbar_wait(&full_bar[st], (i / S) & 1);
@@ -371,21 +402,36 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[st]);  // this warp is done with the stage's scales
       for (int j = 0; j < ntok; ++j) {
-        float acc = 0.f;
+        // four partial sums, so the FMAs of a chunk do not wait on each other
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
         const uint32_t col = buf * acc_cols + j * p.hi_pad;
+        const float4* w4 = reinterpret_cast<const float4*>(sw + j * p.hi_pad);
         for (int hc = 0; hc < p.hi_pad; hc += 32) {
           if (hc + 32 <= p.hi_pad) {
             uint32_t v[32];
             tmem_ld32_sync(lane_addr + col + hc, v);
 #pragma unroll
-            for (int x = 0; x < 32; ++x) acc = fmaf(sw[j * p.hi_pad + hc + x], fmaxf(__uint_as_float(v[x]), 0.f), acc);
+            for (int x = 0; x < 8; ++x) {
+              const float4 w = w4[hc / 4 + x];
+              a0 = fmaf(w.x, fmaxf(__uint_as_float(v[4 * x]), 0.f), a0);
+              a1 = fmaf(w.y, fmaxf(__uint_as_float(v[4 * x + 1]), 0.f), a1);
+              a2 = fmaf(w.z, fmaxf(__uint_as_float(v[4 * x + 2]), 0.f), a2);
+              a3 = fmaf(w.w, fmaxf(__uint_as_float(v[4 * x + 3]), 0.f), a3);
+            }
           } else {
             uint32_t v[16];
             tmem_ld16_sync(lane_addr + col + hc, v);
 #pragma unroll
-            for (int x = 0; x < 16; ++x) acc = fmaf(sw[j * p.hi_pad + hc + x], fmaxf(__uint_as_float(v[x]), 0.f), acc);
+            for (int x = 0; x < 4; ++x) {
+              const float4 w = w4[hc / 4 + x];
+              a0 = fmaf(w.x, fmaxf(__uint_as_float(v[4 * x]), 0.f), a0);
+              a1 = fmaf(w.y, fmaxf(__uint_as_float(v[4 * x + 1]), 0.f), a1);
+              a2 = fmaf(w.z, fmaxf(__uint_as_float(v[4 * x + 2]), 0.f), a2);
+              a3 = fmaf(w.w, fmaxf(__uint_as_float(v[4 * x + 3]), 0.f), a3);
+            }
           }
         }
+        const float acc = (a0 + a1) + (a2 + a3);
         const float out = (s < s_valid[j] && !bad) ? acc * scale_k : -INFINITY;
         if (s < p.ld) p.logits[static_cast<int64_t>(s_tok[j]) * p.ld + s] = out;
       }
