@@ -257,23 +257,21 @@ def main():
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
     t_step = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
-    # per-kernel breakdown from separate steps with events between the kernels
+    # per-kernel breakdown: each phase timed on its own, after its own L2
+    # flush (its inputs are the previous phase's outputs, already in place)
     Kb = max(5, min(K, 50))
-    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Kb)]
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(Kb)]
     for k in range(Kb):
-        flush_l2()
         e = evb[k]
-        e[0].record(stream)
-        step.indexer()
-        e[1].record(stream)
-        step.topk()
-        e[2].record(stream)
-        step.attention()
-        e[3].record(stream)
+        for ph, fn in enumerate((step.indexer, step.topk, step.attention)):
+            flush_l2()
+            e[2 * ph].record(stream)
+            fn()
+            e[2 * ph + 1].record(stream)
     barrier()
     t_idx = [evb[k][0].elapsed_time(evb[k][1]) for k in range(Kb)]
-    t_topk = [evb[k][1].elapsed_time(evb[k][2]) for k in range(Kb)]
-    t_att = [evb[k][2].elapsed_time(evb[k][3]) for k in range(Kb)]
+    t_topk = [evb[k][2].elapsed_time(evb[k][3]) for k in range(Kb)]
+    t_att = [evb[k][4].elapsed_time(evb[k][5]) for k in range(Kb)]
     from deepseek_sparse_attention_fp8_gb300.replicas import aggregate
 
     ms, _, value = aggregate(float(np.mean(t_step)), wl.T, step.device)

@@ -29,7 +29,9 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 192;       // 4 epilogue warps, 1 load warp, 1 MMA warp
+constexpr int kThreads = 320;       // 8 epilogue warps, 1 load warp, 1 MMA warp
+constexpr int kEpiThreads = 256;
+constexpr int kProdWarp = 8, kMmaWarp = 9;
 constexpr int kQuantThreads = 128;
 constexpr int kTileKeys = 128;
 constexpr int kMaxStages = 6;
@@ -109,7 +111,7 @@ struct IndexerParams {
 };
 
 struct SmemOffsets {
-  int k, sc, q, w, total;
+  int k, sc, q, w, part, total;
 };
 __host__ __device__ inline SmemOffsets indexer_smem(int n_cols, int stages) {
   SmemOffsets o;
@@ -117,7 +119,8 @@ __host__ __device__ inline SmemOffsets indexer_smem(int n_cols, int stages) {
   o.sc = o.k + stages * kTileBytes;
   o.q = (o.sc + stages * kTileKeys * 4 + 1023) & ~1023;
   o.w = o.q + n_cols * 128;
-  o.total = o.w + n_cols * 4 + 1024;  // + slack for 1024-byte alignment of the base
+  o.part = o.w + n_cols * 4;
+  o.total = o.part + 2 * kTileKeys * 4 + 1024;  // + slack for 1024-byte alignment of the base
   return o;
 }
 // two CTAs per SM: stages sized so that 2 x smem stays within 228 KB
@@ -127,11 +130,11 @@ __host__ __device__ inline int indexer_stages(int n_cols) { return n_cols <= 64 
 // owns TMEM lanes 32w..32w+31 = keys of the tile); warp 4 loads key tiles
 // (TMA for 128-byte rows, cp.async otherwise); warp 5 issues the MMAs.
 template <int DI>
-__global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __grid_constant__ IndexerParams p,
+__global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __grid_constant__ IndexerParams p,
                                                                      const __grid_constant__ CUtensorMap kmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], acc_full[2], acc_empty[2], q_ready;
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], acc_full[2], acc_empty[2], q_ready, pair_bar[4];
   __shared__ uint32_t tmem_holder;
   __shared__ int s_tok[kMaxTokensPerCta];
   __shared__ int s_valid[kMaxTokensPerCta];
@@ -188,17 +191,17 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
   // warps 0-3 quantise the queries meanwhile (the MMA waits on q_ready).
   // a0 takes 16 (token, head) rows per pass, 8 lanes per row; the loads of
   // every pass are issued before the barrier so their latency overlaps it.
-  constexpr int kQPass = 4;  // passes in flight: 64 rows (up to 4 tokens x 16 heads, or 1 token x 64 heads)
+  constexpr int kQPass = 2;  // passes in flight: 64 rows (up to 4 tokens x 16 heads, or 1 token x 64 heads)
   uint4 qa[kQPass], qb[kQPass];
   float qw[kQPass];
   if (n_comp > 0) {
     if constexpr (DI < 128) {  // row padding past Di is never written by the loads
       for (int i = tid; i < S * kTileBytes / 16; i += kThreads) reinterpret_cast<uint4*>(sk)[i] = make_uint4(0, 0, 0, 0);
     }
-    if (warp < 4) {
+    if (warp < 8) {
 #pragma unroll
       for (int u = 0; u < kQPass; ++u) {
-        const int n = u * 16 + tid / 8, c = tid % 8;
+        const int n = u * 32 + tid / 8, c = tid % 8;
         const int j = n / p.hi_pad, h = n % p.hi_pad;
         qa[u] = make_uint4(0, 0, 0, 0);
         qb[u] = qa[u];
@@ -214,27 +217,28 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
         }
       }
     } else {
-      // block ids of every key this CTA reads (warps 4 and 5)
-      for (int i = tid - 128; i < n_blk; i += 64) {
+      // block ids of every key this CTA reads (warps 8 and 9)
+      for (int i = tid - kEpiThreads; i < n_blk; i += 64) {
         const int lb = blk0 + i;
         s_blk[i] = lb * p.block_size < seq_len ? __ldg(bt_row + lb) : -1;
       }
     }
     if (DI < 128) fence_proxy_async_smem();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
       tmem_alloc(&tmem_holder, tmem_cols);
       tmem_relinquish();
     }
     if (tid == 0) {
       for (int s = 0; s < S; ++s) {
         mbar_init(&full_bar[s], DI == 128 ? 1 : 32);
-        mbar_init(&empty_bar[s], 1 + 4);
+        mbar_init(&empty_bar[s], 1 + 8);
       }
       for (int s = 0; s < 2; ++s) {
         mbar_init(&acc_full[s], 1);
-        mbar_init(&acc_empty[s], 4);
+        mbar_init(&acc_empty[s], 8);
       }
-      mbar_init(&q_ready, 4);
+      mbar_init(&q_ready, 8);
+      for (int q = 0; q < 4; ++q) mbar_init(&pair_bar[q], 2);  // the two warps of a lane group, once per tile
       fence_mbar_init();
     }
   }
@@ -242,14 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   if (n_comp > 0) tmem = tmem_holder;
-  if (n_comp > 0 && warp < 4) {
+  if (n_comp > 0 && warp < 8) {
     // a0: the token block's queries -> the B operand (N rows x 128 B) and
     // the per-column weight w * scale_q
-    for (int base0 = 0; base0 < n_cols; base0 += kQPass * 16) {
+    for (int base0 = 0; base0 < n_cols; base0 += kQPass * 32) {
       if (base0 > 0) {  // more than 64 columns: the later passes load here
 #pragma unroll
         for (int u = 0; u < kQPass; ++u) {
-          const int n = base0 + u * 16 + tid / 8, c = tid % 8;
+          const int n = base0 + u * 32 + tid / 8, c = tid % 8;
           const int j = n / p.hi_pad, h = n % p.hi_pad;
           qa[u] = make_uint4(0, 0, 0, 0);
           qb[u] = qa[u];
@@ -267,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
       }
 #pragma unroll
       for (int u = 0; u < kQPass; ++u) {
-        const int n = base0 + u * 16 + tid / 8, c = tid % 8;
-        if (base0 + u * 16 >= n_cols) break;  // uniform across the four warps
+        const int n = base0 + u * 32 + tid / 8, c = tid % 8;
+        if (n >= n_cols) break;  // uniform within a warp (n_cols is a multiple of 16)
         float scale;
         const uint4 codes = quant_chunk16(qa[u], qb[u], scale);
         *reinterpret_cast<uint4*>(sq + sw128_offset(n, c)) = codes;
@@ -278,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
     fence_proxy_async_smem();  // the MMA reads the codes through the async proxy
     __syncwarp();
     if (lane == 0) mbar_arrive(&q_ready);
-    named_barrier_sync(1, 128);  // every column weight is written before the epilogue reads them
+    named_barrier_sync(1, kEpiThreads);  // every column weight is written before the epilogue reads them
   }
 
   auto abort_now = [&](void) {
@@ -290,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
     return blk >= 0 && blk < p.num_blocks;
   };
 
-  if (n_comp > 0 && warp == 4) {
+  if (n_comp > 0 && warp == kProdWarp) {
     // ---------------- producer
     for (int i = 0; i < n_comp && !s_abort; ++i) {
       const int st = i % S;
@@ -361,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
         cp_async_mbar_arrive(&full_bar[st]);
       }
     }
-  } else if (n_comp > 0 && warp == 5) {
+  } else if (n_comp > 0 && warp == kMmaWarp) {
     // ---------------- MMA issuer
     const uint32_t idesc = idesc_e4m3(128, n_cols);
     if (!mbar_wait(&q_ready, 0) && lane == 0) abort_now();
@@ -386,9 +390,47 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
       __syncwarp();
     }
   } else if (n_comp > 0) {
-    // ---------------- epilogue: thread = key row = TMEM lane
-    const int r = warp * 32 + lane;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // ---------------- epilogue: thread = key row = TMEM lane. Warps w and
+    // w+4 share the lanes 32(w%4)..: with two or more tokens they take
+    // alternate tokens; with one token they take half of the heads each and
+    // warp w adds warp w+4's partial sums through shared memory.
+    const int g = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const bool head_split = ntok == 1 && p.hi_pad % 64 == 0;
+    float* part = reinterpret_cast<float*>(smem + so.part);  // [2][128] second-half sums
+    // sum over heads [h0, h1) of token j (h1 - h0 a multiple of 16)
+    auto head_sum = [&](int buf, int j, int h0, int h1) -> float {
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // independent FMA chains
+      const uint32_t col = buf * acc_cols + j * p.hi_pad;
+      const float4* w4 = reinterpret_cast<const float4*>(sw + j * p.hi_pad);
+      for (int hc = h0; hc < h1; hc += 32) {
+        if (hc + 32 <= h1) {
+          uint32_t v[32];
+          tmem_ld32_sync(lane_addr + col + hc, v);
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            const float4 w = w4[hc / 4 + x];
+            a0 = fmaf(w.x, fmaxf(__uint_as_float(v[4 * x]), 0.f), a0);
+            a1 = fmaf(w.y, fmaxf(__uint_as_float(v[4 * x + 1]), 0.f), a1);
+            a2 = fmaf(w.z, fmaxf(__uint_as_float(v[4 * x + 2]), 0.f), a2);
+            a3 = fmaf(w.w, fmaxf(__uint_as_float(v[4 * x + 3]), 0.f), a3);
+          }
+        } else {
+          uint32_t v[16];
+          tmem_ld16_sync(lane_addr + col + hc, v);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const float4 w = w4[hc / 4 + x];
+            a0 = fmaf(w.x, fmaxf(__uint_as_float(v[4 * x]), 0.f), a0);
+            a1 = fmaf(w.y, fmaxf(__uint_as_float(v[4 * x + 1]), 0.f), a1);
+            a2 = fmaf(w.z, fmaxf(__uint_as_float(v[4 * x + 2]), 0.f), a2);
+            a3 = fmaf(w.w, fmaxf(__uint_as_float(v[4 * x + 3]), 0.f), a3);
+          }
+        }
+      }
+      return (a0 + a1) + (a2 + a3);
+    };
     for (int i = 0; i < n_comp && !s_abort; ++i) {
       const int st = i % S, buf = i % nbuf;
       if (!mbar_wait(&acc_full[buf], (i / nbuf) & 1)) {
@@ -401,39 +443,29 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
       const bool bad = s < seq_len && !block_ok(s);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[st]);  // this warp is done with the stage's scales
-      for (int j = 0; j < ntok; ++j) {
-        // four partial sums, so the FMAs of a chunk do not wait on each other
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-        const uint32_t col = buf * acc_cols + j * p.hi_pad;
-        const float4* w4 = reinterpret_cast<const float4*>(sw + j * p.hi_pad);
-        for (int hc = 0; hc < p.hi_pad; hc += 32) {
-          if (hc + 32 <= p.hi_pad) {
-            uint32_t v[32];
-            tmem_ld32_sync(lane_addr + col + hc, v);
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-              const float4 w = w4[hc / 4 + x];
-              a0 = fmaf(w.x, fmaxf(__uint_as_float(v[4 * x]), 0.f), a0);
-              a1 = fmaf(w.y, fmaxf(__uint_as_float(v[4 * x + 1]), 0.f), a1);
-              a2 = fmaf(w.z, fmaxf(__uint_as_float(v[4 * x + 2]), 0.f), a2);
-              a3 = fmaf(w.w, fmaxf(__uint_as_float(v[4 * x + 3]), 0.f), a3);
-            }
-          } else {
-            uint32_t v[16];
-            tmem_ld16_sync(lane_addr + col + hc, v);
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const float4 w = w4[hc / 4 + x];
-              a0 = fmaf(w.x, fmaxf(__uint_as_float(v[4 * x]), 0.f), a0);
-              a1 = fmaf(w.y, fmaxf(__uint_as_float(v[4 * x + 1]), 0.f), a1);
-              a2 = fmaf(w.z, fmaxf(__uint_as_float(v[4 * x + 2]), 0.f), a2);
-              a3 = fmaf(w.w, fmaxf(__uint_as_float(v[4 * x + 3]), 0.f), a3);
-            }
-          }
+      if (head_split) {
+        const int hh = p.hi_pad / 2;
+        const float mine = head_sum(buf, 0, g * hh, (g + 1) * hh);
+        float* slot = part + (i & 1) * kTileKeys;
+        if (g == 1) slot[r] = mine;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pair_bar[warp & 3]);
+        // both warps arrive once per tile, so neither runs two tiles ahead
+        if (g == 0 && !mbar_wait(&pair_bar[warp & 3], i & 1)) {
+          if (lane == 0) abort_now();
+          break;
         }
-        const float acc = (a0 + a1) + (a2 + a3);
-        const float out = (s < s_valid[j] && !bad) ? acc * scale_k : -INFINITY;
-        if (s < p.ld) p.logits[static_cast<int64_t>(s_tok[j]) * p.ld + s] = out;
+        if (g == 0) {
+          const float acc = mine + slot[r];
+          const float out = (s < s_valid[0] && !bad) ? acc * scale_k : -INFINITY;
+          if (s < p.ld) p.logits[static_cast<int64_t>(s_tok[0]) * p.ld + s] = out;
+        }
+      } else {
+        for (int j = g; j < ntok; j += 2) {  // one token: warp w alone (fewer than 64 head columns)
+          const float acc = head_sum(buf, j, 0, p.hi_pad);
+          const float out = (s < s_valid[j] && !bad) ? acc * scale_k : -INFINITY;
+          if (s < p.ld) p.logits[static_cast<int64_t>(s_tok[j]) * p.ld + s] = out;
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -453,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_logits_kernel(const __gri
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (n_comp > 0 && warp == 5) tmem_dealloc(tmem, tmem_cols);
+  if (n_comp > 0 && warp == kMmaWarp) tmem_dealloc(tmem, tmem_cols);
 }
 
 bool g_smem_set[3] = {false, false, false};
