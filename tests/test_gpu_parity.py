@@ -142,7 +142,7 @@ def test_topk_long_rows_match_full_sort(ld):
     check_topk_sets(got, ref, range(T))
 
 
-@pytest.mark.parametrize("splits", [1, 2, 8, 32])
+@pytest.mark.parametrize("splits", [1, 2, 3, 4, 8, 32])
 def test_attention_splits(splits):
     wl = _wl("decode_small")
     step = DsaStep(wl, num_kv_splits=splits)
