@@ -36,7 +36,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxParts = 8;     // CTAs per row (portable cluster size)
 constexpr int kSegCap = 32768;   // keys of one part staged in shared memory
@@ -59,6 +59,7 @@ struct TopkShared {
   float red_f[2][kWarps];
   uint32_t red_u[3][kWarps];
   uint32_t bsel, above, thr;
+  int32_t qsl_s[kThreads + 1], sl_s[kThreads];  // the batch's query_start_loc and seq_lens (B <= kThreads)
 };
 
 __device__ __forceinline__ uint32_t order_key(float v) {
@@ -94,18 +95,10 @@ __device__ __forceinline__ uint32_t atom_add_cluster_u32(uint32_t addr, uint32_t
 
 // valid(t): the number of leading positions of row t that are ranked. Every
 // thread of the block calls it: the request of token t is the last b with
-// query_start_loc[b] <= t, counted over the block in one round of loads.
-__device__ int valid_length(const int32_t* seq_lens, const int32_t* qsl, int B, int t, int64_t ld) {
-  int cnt = 0;
-  for (int j0 = 0; j0 < B; j0 += kThreads) {
-    const int j = j0 + static_cast<int>(threadIdx.x);
-    cnt += __syncthreads_count(j < B && __ldg(qsl + j) <= t);
-  }
-  const int b = max(0, cnt - 1);
-  const int q0 = __ldg(qsl + b), q1 = __ldg(qsl + b + 1);
-  const int64_t v = static_cast<int64_t>(__ldg(seq_lens + b)) - (q1 - q0) + (t - q0) + 1;
-  return static_cast<int>(max(static_cast<int64_t>(0), min(v, ld)));
-}
+// query_start_loc[b] <= t, counted over the block. Up to kThreads requests,
+// query_start_loc and seq_lens arrive in one round of loads.
+struct TopkShared;
+__device__ int valid_length(const int32_t* seq_lens, const int32_t* qsl, int B, int t, int64_t ld, TopkShared& sh);
 
 // Exclusive block scan of `v`; returns the prefix and sets `total`. Two
 // 32-bit counts can travel packed in one 64-bit value.
@@ -134,6 +127,33 @@ __device__ __forceinline__ uint64_t block_exclusive_scan(uint64_t v, uint64_t& t
   const uint64_t r = before_warp + x - v;
   __syncthreads();  // sh.scan is reused by the next call
   return r;
+}
+
+__device__ int valid_length(const int32_t* seq_lens, const int32_t* qsl, int B, int t, int64_t ld, TopkShared& sh) {
+  const int tid = static_cast<int>(threadIdx.x);
+  int b, q0, q1, sl;
+  if (B <= kThreads) {
+    const int qv = tid <= B ? __ldg(qsl + tid) : 0;
+    const int sv = tid < B ? __ldg(seq_lens + tid) : 0;
+    if (tid <= B) sh.qsl_s[tid] = qv;
+    if (tid < B) sh.sl_s[tid] = sv;
+    b = max(0, __syncthreads_count(tid < B && qv <= t) - 1);
+    q0 = sh.qsl_s[b];
+    q1 = sh.qsl_s[b + 1];
+    sl = sh.sl_s[b];
+  } else {
+    int cnt = 0;
+    for (int j0 = 0; j0 < B; j0 += kThreads) {
+      const int j = j0 + tid;
+      cnt += __syncthreads_count(j < B && __ldg(qsl + j) <= t);
+    }
+    b = max(0, cnt - 1);
+    q0 = __ldg(qsl + b);
+    q1 = __ldg(qsl + b + 1);
+    sl = __ldg(seq_lens + b);
+  }
+  const int64_t v = static_cast<int64_t>(sl) - (q1 - q0) + (t - q0) + 1;
+  return static_cast<int>(max(static_cast<int64_t>(0), min(v, ld)));
 }
 
 // The bin of the row histogram `ghist` holding the `need`-th largest element
@@ -183,24 +203,39 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   const int P = p.parts;
   const int r = static_cast<int>(cluster_ctarank());
   const int t = blockIdx.x / P;
-  const int n = valid_length(p.seq_lens, p.qsl, p.B, t, p.ld);
   const int k = p.k;
   int32_t* out = p.out + static_cast<int64_t>(t) * k;
+  const float* row = p.logits + static_cast<int64_t>(t) * p.ld;
+  // The row's parts are cut by ld, so the first values are loaded before
+  // valid(t) is known; positions at or past valid(t) are ignored afterwards.
+  const int ld = static_cast<int>(p.ld);
+  const int seg = (ld + P - 1) / P;
+  const int s0 = min(ld, r * seg);
+  const int m_ld = min(ld, s0 + seg) - s0;
+  float v_first[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int i = u * kThreads + tid;
+    v_first[u] = i < m_ld ? __ldg(row + s0 + i) : 0.f;
+  }
+  const int n = valid_length(p.seq_lens, p.qsl, p.B, t, p.ld, sh);
   if (n <= k) {  // every valid position, then -1 (the same branch for the whole cluster)
     const int o0 = static_cast<int>(static_cast<int64_t>(r) * k / P);
     const int o1 = static_cast<int>(static_cast<int64_t>(r + 1) * k / P);
     for (int i = o0 + tid; i < o1; i += kThreads) out[i] = i < n ? i : -1;
     return;
   }
-  const float* row = p.logits + static_cast<int64_t>(t) * p.ld;
-  const int seg = (n + P - 1) / P;
-  const int s0 = min(n, r * seg);
-  const int m = min(n, s0 + seg) - s0;  // this part's length (may be 0)
+  const int m = max(0, min(n - s0, m_ld));  // this part's valid length (may be 0)
   auto key_at = [&](int i) -> uint32_t {
     if constexpr (kCached) return kc[i];
     else return order_key(__ldg(row + s0 + i));
   };
   auto remote = [&](const void* ptr, int q) -> uint32_t { return mapa_shared(smem_u32(ptr), static_cast<uint32_t>(q)); };
+  // barrier over the row's CTAs (a CTA barrier when the row has one CTA)
+  auto row_sync = [&]() {
+    if (P == 1) __syncthreads();
+    else cluster_sync_all();
+  };
 
   // ---- 1. bin range: the finite min and max of 1024 evenly spaced samples of
   // the row, the same in every CTA of the row
@@ -253,7 +288,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int i = base + u * kThreads + tid;
-      v[u] = i < m ? __ldg(row + s0 + i) : 0.f;
+      v[u] = base == 0 ? v_first[u] : (i < m ? __ldg(row + s0 + i) : 0.f);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -267,13 +302,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   }
   const int sl0 = r * (kBins / P), sl1 = (r + 1) * (kBins / P);
   auto reduce_hist = [&]() {
-    cluster_sync_all();  // every local histogram is complete
+    row_sync();  // every local histogram is complete
     for (int b = sl0 + tid; b < sl1; b += kThreads) {
       uint32_t s = 0;
       for (int q = 0; q < P; ++q) s += ld_cluster_u32(remote(&sh.hist[b], q));
       for (int q = 0; q < P; ++q) st_cluster_u32(remote(&sh.ghist[b], q), s);
     }
-    cluster_sync_all();  // every CTA holds the whole row histogram
+    row_sync();  // every CTA holds the whole row histogram
   };
   reduce_hist();
   find_bin(sh, static_cast<uint32_t>(k));
@@ -343,7 +378,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
         st_cluster_u32(remote(&sh.cand_pos[slot], q), static_cast<uint32_t>(sh.loc_pos[j]));
       }
     }
-    cluster_sync_all();  // after this, no CTA reads or writes another's shared memory
+    row_sync();  // after this, no CTA reads or writes another's shared memory
                          // unless the bin is refined below
   }
 
@@ -417,7 +452,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
       st_cluster_u32(remote(&sh.part_gt[r], tid), static_cast<uint32_t>(tot));
       st_cluster_u32(remote(&sh.part_eq[r], tid), static_cast<uint32_t>(tot >> 32));
     }
-    cluster_sync_all();  // no shared-memory access between the CTAs after this
+    row_sync();  // no shared-memory access between the CTAs after this
     for (int q = 0; q < r; ++q) {
       g_base += sh.part_gt[q];
       e_base += sh.part_eq[q];
@@ -441,11 +476,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
 
 bool g_smem = false, g_smem_u = false;
 
-// CTAs per row: as many as fill the GPU once (at most 8), and enough that a
-// part fits the shared-memory stage where possible.
+// CTAs per row: more only for long rows (at least 8192 keys per CTA) while
+// they fill the GPU once (at most 8), and enough that a part fits the
+// shared-memory stage where possible. A cluster barrier costs about as much
+// as a short row's whole selection, so short rows keep one CTA.
 int parts_for(int32_t T, int64_t ld) {
   int P = 1;
-  while (P < kMaxParts && static_cast<int64_t>(T) * P * 2 <= num_sms() && (ld + 2 * P - 1) / (2 * P) >= 1024) P *= 2;
+  while (P < kMaxParts && static_cast<int64_t>(T) * P * 2 <= num_sms() && (ld + 2 * P - 1) / (2 * P) >= 8192) P *= 2;
   while (P < kMaxParts && (ld + P - 1) / P > kSegCap) P *= 2;
   return P;
 }
