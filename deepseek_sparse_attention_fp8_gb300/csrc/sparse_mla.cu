@@ -53,27 +53,35 @@ static_assert(kMaxSlots <= 256 * 8, "the softmax warps resolve all slots in one 
 static_assert(kQStage + 2 <= kStages, "q staging needs two KV stages");
 constexpr int kXPitch = 64 * 2 + 16;      // bytes per row of an exchange buffer (fp16 scores)
 
-// kPair: the two CTAs of a cluster split the Dk dims (rank 0: K-blocks
-// [0, kNkb0), rank 1: the rest) and the value dims (rank r: values
-// [r*kDvc, (r+1)*kDvc)), and exchange partial scores through DSMEM.
+// kPair: the two CTAs of a cluster split the Dk dims and the value dims:
+// rank r owns value dims [r*kDvc, (r+1)*kDvc) = K-blocks [4r, 4r+4) (64 dims
+// each), and half of the rope dims, [512 + 32r, 544 + 32r), which enter QK
+// only; both gather 576 bytes of every row. They exchange partial scores
+// through DSMEM.
 template <int DK, int DV>
 struct MlaCfg;
 template <>
 struct MlaCfg<576, 512> {
   static constexpr bool kPair = true;
-  static constexpr int kNkb0 = 4, kNkb1 = 5, kMaxNkb = 5, kDvc = 256, kTmemCols = 512;
+  static constexpr int kNkb = 4, kMaxNkb = 4, kDvc = 256, kTmemCols = 512;
+  static constexpr bool kRopeHalf = true;  // plus a 32-dim rope half-block (64-byte rows)
+  static constexpr int kRopeX = 512;       // first rope dim
 };
 template <>
 struct MlaCfg<80, 64> {
   static constexpr bool kPair = false;
-  static constexpr int kNkb0 = 2, kNkb1 = 0, kMaxNkb = 2, kDvc = 64, kTmemCols = 256;
+  static constexpr int kNkb = 2, kMaxNkb = 2, kDvc = 64, kTmemCols = 256;
+  static constexpr bool kRopeHalf = false;
+  static constexpr int kRopeX = 0;
 };
 
 template <int DK, int DV>
 struct MlaSmem {
   using C = MlaCfg<DK, DV>;
   static constexpr int kKvKb = kTileKeys * 128;  // one 64-dim K-block of a KV tile
-  static constexpr int kKvStage = C::kMaxNkb * kKvKb;
+  static constexpr int kKvHalf = C::kMaxNkb * kKvKb;  // the rope half-block: 64 keys x 64 B (SWIZZLE_64B)
+  static constexpr int kKvStage = kKvHalf + (C::kRopeHalf ? kTileKeys * 64 : 0);
+  static constexpr int kQHalf = C::kRopeHalf ? 128 * 64 : 0;  // q's rope half: 128 heads x 64 B
   static constexpr int kKv = 0;
   static constexpr int kP = kKv + kStages * kKvStage;
   static constexpr int kX = kP + 16384;
@@ -83,7 +91,7 @@ struct MlaSmem {
   static constexpr int kCoord = kLive + kStages * kTileKeys;
   static constexpr int kRed = kCoord + kStages * kTileKeys * 4;
   static constexpr int kTotal = kRed + 6 * 128 * 4 + 1024;
-  static_assert(C::kMaxNkb * 16384 <= 2 * kKvStage, "q staging does not fit in two KV stages");
+  static_assert(C::kMaxNkb * 16384 + kQHalf <= 2 * kKvStage, "q staging does not fit in two KV stages");
 };
 
 struct MlaParams {
@@ -128,7 +136,9 @@ __device__ __forceinline__ int find_request(const int32_t* qsl, int B, int t) {
 template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_constant__ MlaParams p,
                                                                  const __grid_constant__ CUtensorMap qmap,
-                                                                 const __grid_constant__ CUtensorMap kvmap) {
+                                                                 const __grid_constant__ CUtensorMap kvmap,
+                                                                 const __grid_constant__ CUtensorMap qmap64,
+                                                                 const __grid_constant__ CUtensorMap kvmap64) {
   using C = MlaCfg<DK, DV>;
   using L = MlaSmem<DK, DV>;
   constexpr int kSplitDv = C::kPair ? 2 : 1;
@@ -148,8 +158,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   const int r = C::kPair ? static_cast<int>(cluster_ctarank()) : 0;
   const int j = (blockIdx.x / kSplitDv) % p.splits;
   const int t = blockIdx.x / (kSplitDv * p.splits);
-  const int kb0 = r == 0 ? 0 : C::kNkb0;          // first K-block (64 dims) this CTA owns
-  const int nkb = r == 0 ? C::kNkb0 : C::kNkb1;   // K-blocks this CTA owns
+  const int kb0 = r * C::kNkb;                     // first K-block (64 dims) this CTA owns
+  constexpr int nkb = C::kNkb;                     // K-blocks this CTA owns
+  const int rope_x = C::kRopeX + 32 * r;           // its rope half (dims), when there is one
 
   uint8_t* kv_sm = smem + L::kKv;
   uint8_t* p_sm = smem + L::kP;
@@ -233,9 +244,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   if (tid == kProdWarp0 * 32) {  // first producer thread
     prefetch_tmap(&qmap);
     prefetch_tmap(&kvmap);
-    mbar_arrive_expect_tx(&q_full, nkb * 16384);
+    if constexpr (C::kRopeHalf) {
+      prefetch_tmap(&qmap64);
+      prefetch_tmap(&kvmap64);
+    }
+    mbar_arrive_expect_tx(&q_full, nkb * 16384 + L::kQHalf);
     for (int kb = 0; kb < nkb; ++kb)
       tma_load_3d(smem_u32(q_stage + kb * 16384), &qmap, &q_full, (kb0 + kb) * 64, 0, t);
+    if constexpr (C::kRopeHalf) tma_load_3d(smem_u32(q_stage + nkb * 16384), &qmap64, &q_full, rope_x, 0, t);
   }
   if (warp < 8) {
     // the split's top-k slots -> physical rows (-1: empty or invalid)
@@ -286,6 +302,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
           tmem_st16(lane_q + kb * 32 + half * 16, v);
         }
       }
+      if constexpr (C::kRopeHalf) {
+        if (warp >> 2 == (nkb & 1)) {  // the rope half: 64-byte rows, chunk c at c ^ ((row >> 1) & 3)
+          uint32_t v[16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 u = *reinterpret_cast<const uint4*>(q_stage + nkb * 16384 + hq * 64 + ((c ^ ((hq >> 1) & 3)) << 4));
+            v[4 * c] = u.x;
+            v[4 * c + 1] = u.y;
+            v[4 * c + 2] = u.z;
+            v[4 * c + 3] = u.w;
+          }
+          tmem_st16(lane_q + nkb * 32, v);
+        }
+      }
       tmem_st_wait();
       fence_proxy_async_smem();  // the staging stages are refilled by TMA next
     }
@@ -300,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     // ---------------- producer: 4 warps, 16 keys each; 4-row TMA gathers of
     // this CTA's K-blocks only
     const int pw = warp - kProdWarp0;
-    const uint32_t tile_bytes = kTileKeys * nkb * 128;
+    const uint32_t tile_bytes = kTileKeys * (nkb * 128 + (C::kRopeHalf ? 64 : 0));
     int issued = 0;
     for (int i = 0; i < n_tiles && !s_abort; ++i) {
       const int st = i % kStages;
@@ -332,6 +362,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
         const int* cs = coord_sm + st * kTileKeys + 4 * g;
         tma_gather4(smem_u32(kv_sm + st * L::kKvStage + kb * L::kKvKb + g * 512), &kvmap, &kv_full[st],
                     (kb0 + kb) * 64, cs[0], cs[1], cs[2], cs[3]);
+      } else if (C::kRopeHalf && lane < 4 * nkb + 4) {  // the rope half of the same 4-row groups
+        const int g = pw * 4 + (lane & 3);
+        const int* cs = coord_sm + st * kTileKeys + 4 * g;
+        tma_gather4(smem_u32(kv_sm + st * L::kKvStage + L::kKvHalf + g * 256), &kvmap64, &kv_full[st], rope_x, cs[0],
+                    cs[1], cs[2], cs[3]);
       }
       issued = i + 1;
     }
@@ -355,12 +390,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       // descriptors differ only in the start-address field (16-byte units)
       const uint64_t d0 = smem_desc(smem_u32(kv_sm + st * L::kKvStage), 16, 1024, kSwizzle128B);
 #pragma unroll
-      for (int kb = 0; kb < C::kMaxNkb; ++kb) {
-        if (kb >= nkb) break;
+      for (int kb = 0; kb < nkb; ++kb) {
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4)
           mma_bf16_ts(tmem + kColS, tmem + kColQ + (kb * 4 + k4) * 8,
                       d0 + static_cast<uint64_t>((kb * L::kKvKb + k4 * 32) >> 4), idesc_qk, (kb | k4) ? 1u : 0u);
+      }
+      if constexpr (C::kRopeHalf) {  // 64-byte rows: SWIZZLE_64B, 8-row groups 512 bytes apart
+        const uint64_t dh = smem_desc(smem_u32(kv_sm + st * L::kKvStage + L::kKvHalf), 16, 512, kSwizzle64B);
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2)
+          mma_bf16_ts(tmem + kColS, tmem + kColQ + (nkb * 4 + k2) * 8, dh + static_cast<uint64_t>((k2 * 32) >> 4),
+                      idesc_qk, 1u);
       }
       mma_commit(&s_full[i & 1]);
     };
@@ -745,22 +786,27 @@ int dv_split_for(int Dv) { return Dv == 512 ? 2 : 1; }
 dsa_status_t launch_mla(const MlaParams& p, const void* q, const void* kv, int Dk, int Dv, cudaStream_t s) {
   const int64_t grid = static_cast<int64_t>(p.T) * p.splits * dv_split_for(Dv);
   if (grid > 0x7FFFFFFF) return fail(DSA_ERR_UNSUPPORTED, "sparse_mla: grid too large");
-  CUtensorMap qmap, kvmap;
-  {
-    const uint64_t dims[3] = {static_cast<uint64_t>(Dk), static_cast<uint64_t>(p.H), static_cast<uint64_t>(p.T)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(Dk) * 2, static_cast<uint64_t>(p.H) * Dk * 2};
-    const uint32_t box[3] = {64, 128, 1};
-    dsa_status_t st = make_tmap(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box,
-                                CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != DSA_OK) return st;
-  }
-  {
-    const uint64_t dims[2] = {static_cast<uint64_t>(Dk), static_cast<uint64_t>(std::max(p.total_rows, 1))};
-    const uint64_t strides[1] = {static_cast<uint64_t>(Dk) * 2};
-    const uint32_t box[2] = {64, 1};
-    dsa_status_t st = make_tmap(&kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv, dims, strides, box,
-                                CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != DSA_OK) return st;
+  // q and the latent rows, each as 64-dim blocks (128-byte rows, SWIZZLE_128B)
+  // and, for the rope dims split between the two CTAs, as 32-dim half-blocks
+  // (64-byte rows, SWIZZLE_64B)
+  CUtensorMap qmap, kvmap, qmap64, kvmap64;
+  for (int half = 0; half < 2; ++half) {
+    const uint32_t w = half ? 32 : 64;
+    const CUtensorMapSwizzle sw = half ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    {
+      const uint64_t dims[3] = {static_cast<uint64_t>(Dk), static_cast<uint64_t>(p.H), static_cast<uint64_t>(p.T)};
+      const uint64_t strides[2] = {static_cast<uint64_t>(Dk) * 2, static_cast<uint64_t>(p.H) * Dk * 2};
+      const uint32_t box[3] = {w, 128, 1};
+      dsa_status_t st = make_tmap(half ? &qmap64 : &qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box, sw);
+      if (st != DSA_OK) return st;
+    }
+    {
+      const uint64_t dims[2] = {static_cast<uint64_t>(Dk), static_cast<uint64_t>(std::max(p.total_rows, 1))};
+      const uint64_t strides[1] = {static_cast<uint64_t>(Dk) * 2};
+      const uint32_t box[2] = {w, 1};
+      dsa_status_t st = make_tmap(half ? &kvmap64 : &kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv, dims, strides, box, sw);
+      if (st != DSA_OK) return st;
+    }
   }
   dsa_status_t st;
   if (Dk == 576) {
@@ -781,12 +827,13 @@ dsa_status_t launch_mla(const MlaParams& p, const void* q, const void* kv, int D
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel<576, 512>, p, qmap, kvmap);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel<576, 512>, p, qmap, kvmap, qmap64, kvmap64);
     if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "sparse_mla_kernel launch failed: %s", cudaGetErrorString(e));
   } else {
     st = allow_smem(sparse_mla_kernel<80, 64>, MlaSmem<80, 64>::kTotal, g_smem_tiny);
     if (st != DSA_OK) return st;
-    sparse_mla_kernel<80, 64><<<static_cast<unsigned>(grid), kThreads, MlaSmem<80, 64>::kTotal, s>>>(p, qmap, kvmap);
+    sparse_mla_kernel<80, 64><<<static_cast<unsigned>(grid), kThreads, MlaSmem<80, 64>::kTotal, s>>>(p, qmap, kvmap, qmap64,
+                                                                                                       kvmap64);
   }
   return check_launch("sparse_mla_kernel");
 }
