@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   // softmax group waits on phases of its own tiles only
   __shared__ uint64_t s_full[2], s_free, p_full, o_done[2], o_final, q_full, q_ready, rows_ready, m_bar[2], epi_bar;
   __shared__ uint32_t tmem_holder;
+  __shared__ int s_qsl[kThreads + 1], s_sl[kThreads];  // the batch's query_start_loc and seq_lens (B <= kThreads)
   __shared__ int s_last_live;
   __shared__ volatile int s_abort;
 
@@ -210,18 +211,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   // Launched as a programmatic dependent: everything above touches no global
   // memory; from here on the previous kernel's results are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int b = find_request(p.qsl, p.B, t);
-  const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1);
-  int64_t valid64 = static_cast<int64_t>(__ldg(p.seq_lens + b)) - (q1 - q0) + (t - q0) + 1;
-  const int64_t cap = static_cast<int64_t>(p.bt_stride) * p.block_size;
-  if (valid64 > cap || valid64 < 1) {
-    if (tid == 0 && r == 0 && j == 0) report(p.dev_status, DSA_DEVERR_SEQ_LEN);
-    valid64 = max(static_cast<int64_t>(0), min(valid64, cap));
-  }
-  const int valid = static_cast<int>(valid64);
   const int slot0 = j * p.per_split;
   const int n_slots = max(0, min(p.K, slot0 + p.per_split) - slot0);
-  // the softmax warps load their top-k slots first
+  // the softmax warps load their top-k slots first; meanwhile the request of
+  // token t (the last b with query_start_loc[b] <= t) is found in one round of
+  // loads when the batch has at most kThreads requests
   const int32_t* idx_row = p.topk + static_cast<int64_t>(t) * p.K + slot0;
   int idx[8];
   if (warp < 8) {
@@ -231,6 +225,29 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       idx[u] = sl < n_slots ? __ldg(idx_row + sl) : -1;
     }
   }
+  int b, q0, q1, sl_b;
+  if (p.B <= kThreads) {
+    const int qv = tid <= p.B ? __ldg(p.qsl + tid) : 0;
+    const int sv = tid < p.B ? __ldg(p.seq_lens + tid) : 0;
+    if (tid <= p.B) s_qsl[tid] = qv;
+    if (tid < p.B) s_sl[tid] = sv;
+    b = max(0, __syncthreads_count(tid < p.B && qv <= t) - 1);
+    q0 = s_qsl[b];
+    q1 = s_qsl[b + 1];
+    sl_b = s_sl[b];
+  } else {
+    b = find_request(p.qsl, p.B, t);
+    q0 = __ldg(p.qsl + b);
+    q1 = __ldg(p.qsl + b + 1);
+    sl_b = __ldg(p.seq_lens + b);
+  }
+  int64_t valid64 = static_cast<int64_t>(sl_b) - (q1 - q0) + (t - q0) + 1;
+  const int64_t cap = static_cast<int64_t>(p.bt_stride) * p.block_size;
+  if (valid64 > cap || valid64 < 1) {
+    if (tid == 0 && r == 0 && j == 0) report(p.dev_status, DSA_DEVERR_SEQ_LEN);
+    valid64 = max(static_cast<int64_t>(0), min(valid64, cap));
+  }
+  const int valid = static_cast<int>(valid64);
 
   auto abort_now = [&](void) {
     s_abort = 1;

@@ -142,6 +142,26 @@ def test_topk_long_rows_match_full_sort(ld):
     check_topk_sets(got, ref, range(T))
 
 
+def test_many_requests():
+    """More requests than one CTA has threads: the kernels find a token's
+    request by a search over query_start_loc instead of a single round of
+    loads. Sampled tokens against the oracle."""
+    lens = [64 + (i * 37) % 200 for i in range(450)]
+    wl = make_workload("decode_b32_l8192", B=len(lens), lens=lens, index_topk=128)
+    step = DsaStep(wl)
+    step.logits.fill_(float("nan"))
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) == 0
+    rows = [0, 223, 449]
+    logits = step.logits.cpu().numpy()
+    check_logits(logits, oracle_logits(wl, rows=rows), rows)
+    idx = step.topk_idx.cpu().numpy()
+    check_topk_sets(idx, O.topk(logits, wl.seq_lens, wl.query_start_loc, wl.index_topk, rows=rows), rows)
+    ref, ref_lse = oracle_attention(wl, idx, rows=rows)
+    check_attention(step.out.float().cpu().numpy(), ref, np.array(rows), step.lse.cpu().numpy(), ref_lse)
+
+
 @pytest.mark.parametrize("splits", [1, 2, 3, 4, 8, 32])
 def test_attention_splits(splits):
     wl = _wl("decode_small")
