@@ -474,6 +474,169 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   }
 }
 
+// One CTA per row, the row in registers (rows of up to 32 * VPT * 32 keys).
+// Warp w owns the contiguous run [w * 32 * VPT, (w + 1) * 32 * VPT), lane l
+// its keys at w * 32 * VPT + 32 u + l, so loads are coalesced and the ordered
+// compaction needs only ballots within a warp and one scan over the warps.
+// The bins span the row's exact finite range; the steps are those of
+// topk_kernel with P = 1.
+template <int VPT>
+__global__ void __launch_bounds__(kThreads) topk_row_kernel(const TopkParams p) {
+  __shared__ TopkShared sh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int t = blockIdx.x;
+  const int k = p.k;
+  int32_t* out = p.out + static_cast<int64_t>(t) * k;
+  const float* row = p.logits + static_cast<int64_t>(t) * p.ld;
+  const int ld = static_cast<int>(p.ld);
+  const int base = warp * 32 * VPT + lane;  // position of key[0]; key[u] sits at base + 32 u
+  uint32_t key[VPT];
+#pragma unroll
+  for (int u = 0; u < VPT; ++u) key[u] = base + 32 * u < ld ? order_key(__ldg(row + base + 32 * u)) : 0u;
+  const int n = valid_length(p.seq_lens, p.qsl, p.B, t, p.ld, sh);
+  if (n <= k) {
+    for (int i = tid; i < k; i += kThreads) out[i] = i < n ? i : -1;
+    return;
+  }
+  auto valid = [&](int u) { return base + 32 * u < n; };
+
+  // ---- exact finite range of the row; histogram over 2048 bins linear in it
+  float lo = INFINITY, hi = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < VPT; ++u) {
+    const float v = key_value(key[u]);
+    if (valid(u) && isfinite(v)) {
+      lo = fminf(lo, v);
+      hi = fmaxf(hi, v);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
+    hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, off));
+  }
+  if (lane == 0) {
+    sh.red_f[0][warp] = lo;
+    sh.red_f[1][warp] = hi;
+  }
+  for (int b = tid; b < kBins; b += kThreads) sh.ghist[b] = 0u;
+  if (tid == 0) sh.cand_n = 0u;
+  __syncthreads();
+  lo = INFINITY;
+  hi = -INFINITY;
+#pragma unroll 8
+  for (int w = 0; w < kWarps; ++w) {
+    lo = fminf(lo, sh.red_f[0][w]);
+    hi = fmaxf(hi, sh.red_f[1][w]);
+  }
+  float inv_w = hi > lo ? static_cast<float>(kBins) / (hi - lo) : 0.f;
+  if (!isfinite(inv_w)) inv_w = 0.f;
+  if (!(lo <= hi)) lo = 0.f;
+#pragma unroll
+  for (int u = 0; u < VPT; ++u)
+    if (valid(u)) atomicAdd(&sh.ghist[lin_bin(key_value(key[u]), lo, inv_w)], 1u);
+  __syncthreads();
+  find_bin(sh, static_cast<uint32_t>(k));
+  const int bsel = static_cast<int>(sh.bsel);
+  const uint32_t c = sh.ghist[bsel];
+  const bool direct = c <= static_cast<uint32_t>(kCandCap);
+  int need = k - static_cast<int>(sh.above);
+
+  // ---- the threshold key within the bin
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+  for (int u = 0; u < VPT; ++u) {
+    if (!valid(u) || lin_bin(key_value(key[u]), lo, inv_w) != bsel) continue;
+    kmin = min(kmin, key[u]);
+    kmax = max(kmax, key[u]);
+    if (direct) {
+      const uint32_t slot = atomicAdd(&sh.cand_n, 1u);
+      sh.cand_key[slot] = key[u];
+      sh.cand_pos[slot] = base + 32 * u;
+    }
+  }
+  uint32_t thr;
+  if (direct) {
+    __syncthreads();
+    if (tid < static_cast<int>(c)) {
+      const uint32_t kk = sh.cand_key[tid];
+      const int pos = sh.cand_pos[tid];
+      int rank = 0;
+      for (int j = 0; j < static_cast<int>(c); ++j) {
+        const uint32_t kj = sh.cand_key[j];
+        rank += (kj > kk) || (kj == kk && sh.cand_pos[j] < pos);
+      }
+      if (rank == need - 1) sh.thr = kk;
+    }
+    __syncthreads();
+    thr = sh.thr;
+    need -= __syncthreads_count(tid < static_cast<int>(c) && sh.cand_key[tid] > thr);
+  } else {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, off));
+      kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, off));
+    }
+    if (lane == 0) {
+      sh.red_u[0][warp] = kmin;
+      sh.red_u[1][warp] = kmax;
+    }
+    __syncthreads();
+    uint32_t klo = 0xFFFFFFFFu, khi = 0u;
+    for (int w = 0; w < kWarps; ++w) {
+      klo = min(klo, sh.red_u[0][w]);
+      khi = max(khi, sh.red_u[1][w]);
+    }
+    // refine over the bin's key interval until it holds one key
+    while (klo < khi) {
+      const uint64_t R = static_cast<uint64_t>(khi - klo) + 1;
+      __syncthreads();  // every thread has read the previous level's histogram
+      for (int b = tid; b < kBins; b += kThreads) sh.ghist[b] = 0u;
+      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < VPT; ++u)
+        if (valid(u) && key[u] >= klo && key[u] <= khi)
+          atomicAdd(&sh.ghist[static_cast<int>((static_cast<uint64_t>(key[u] - klo) * kBins) / R)], 1u);
+      __syncthreads();
+      find_bin(sh, static_cast<uint32_t>(need));
+      const uint64_t b = sh.bsel;
+      need -= static_cast<int>(sh.above);
+      const uint32_t nlo = klo + static_cast<uint32_t>((b * R + kBins - 1) / kBins);
+      const uint32_t nhi = klo + static_cast<uint32_t>(((b + 1) * R + kBins - 1) / kBins) - 1u;
+      klo = nlo;
+      khi = nhi;
+    }
+    thr = klo;
+  }
+
+  // ---- ordered compaction: warp counts by ballots, one scan over the warps
+  uint32_t cg = 0, ce = 0;
+#pragma unroll
+  for (int u = 0; u < VPT; ++u) {
+    cg += __popc(__ballot_sync(0xFFFFFFFFu, valid(u) && key[u] > thr));
+    ce += __popc(__ballot_sync(0xFFFFFFFFu, valid(u) && key[u] == thr));
+  }
+  uint64_t tot;
+  const uint64_t wpre = block_exclusive_scan(lane == 0 ? (static_cast<uint64_t>(cg) | (static_cast<uint64_t>(ce) << 32)) : 0ull,
+                                             tot, sh);
+  const uint64_t wbefore = __shfl_sync(0xFFFFFFFFu, wpre, 0);
+  uint32_t g = static_cast<uint32_t>(wbefore), e = static_cast<uint32_t>(wbefore >> 32);
+  const uint32_t nq = static_cast<uint32_t>(need);
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int u = 0; u < VPT; ++u) {
+    const bool gt = valid(u) && key[u] > thr, eq = valid(u) && key[u] == thr;
+    const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), be = __ballot_sync(0xFFFFFFFFu, eq);
+    const uint32_t gi = g + __popc(bg & lt), ei = e + __popc(be & lt);
+    if (gt) out[gi + min(ei, nq)] = base + 32 * u;
+    if (eq && ei < nq) out[gi + ei] = base + 32 * u;
+    g += __popc(bg);
+    e += __popc(be);
+  }
+}
+
 bool g_smem = false, g_smem_u = false;
 
 // CTAs per row: more only for long rows (at least 8192 keys per CTA) while
@@ -523,6 +686,21 @@ extern "C" dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t*
   p.k = index_topk;
   p.out = topk_idx;
   p.parts = parts_for(T, ld);
+  if (p.parts == 1 && ld <= 32 * 32 * 32) {  // one CTA per row, the row in registers
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(T));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = ld <= 32 * 8 * 32 ? cudaLaunchKernelEx(&cfg, topk_row_kernel<8>, p)
+                                            : cudaLaunchKernelEx(&cfg, topk_row_kernel<32>, p);
+    if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "topk_row_kernel launch failed: %s", cudaGetErrorString(e));
+    return DSA_OK;
+  }
   const int64_t seg = (ld + p.parts - 1) / p.parts;
   const bool cached = seg <= kSegCap;
   const int smem = cached ? static_cast<int>(seg * 4) : 0;
