@@ -295,6 +295,9 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   };
 
   if (n_comp > 0 && warp == kProdWarp) {
+    // keys that later token blocks of the request read again stay in L2
+    const bool keep_keys = p.n_tb > 1;
+    const uint64_t l2_keep = l2_policy_evict_last();
     // ---------------- producer
     for (int i = 0; i < n_comp && !s_abort; ++i) {
       const int st = i % S;
@@ -324,7 +327,11 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
           mbar_arrive_expect_tx(&full_bar[st], bytes);
           for (int u = 0; u < 2; ++u) {
             if (blk_u[u] < 0) continue;
-            tma_load_3d(smem_u32(sk + st * kTileBytes + u * 8192), &kmap, &full_bar[st], 0, off_u[u], blk_u[u]);
+            if (keep_keys)
+              tma_load_3d_hint(smem_u32(sk + st * kTileBytes + u * 8192), &kmap, &full_bar[st], 0, off_u[u], blk_u[u],
+                               l2_keep);
+            else
+              tma_load_3d(smem_u32(sk + st * kTileBytes + u * 8192), &kmap, &full_bar[st], 0, off_u[u], blk_u[u]);
             bulk_copy_g2s(smem_u32(ssc + st * kTileKeys + u * 64),
                           p.k_cache + static_cast<int64_t>(blk_u[u]) * p.k_block_stride +
                               static_cast<int64_t>(p.block_size) * 128 + off_u[u] * 4,
@@ -458,13 +465,13 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
         if (g == 0) {
           const float acc = mine + slot[r];
           const float out = (s < s_valid[0] && !bad) ? acc * scale_k : -INFINITY;
-          if (s < p.ld) p.logits[static_cast<int64_t>(s_tok[0]) * p.ld + s] = out;
+          if (s < p.ld) __stcs(p.logits + static_cast<int64_t>(s_tok[0]) * p.ld + s, out);
         }
       } else {
         for (int j = g; j < ntok; j += 2) {  // one token: warp w alone (fewer than 64 head columns)
           const float acc = head_sum(buf, j, 0, p.hi_pad);
           const float out = (s < s_valid[j] && !bad) ? acc * scale_k : -INFINITY;
-          if (s < p.ld) p.logits[static_cast<int64_t>(s_tok[j]) * p.ld + s] = out;
+          if (s < p.ld) __stcs(p.logits + static_cast<int64_t>(s_tok[j]) * p.ld + s, out);
         }
       }
       tc_fence_before();
@@ -478,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
     for (int tile = t_begin + n_comp; tile < t_end; ++tile) {
       const int s = tile * kTileKeys + tid;
       if (s < p.ld)
-        for (int j = 0; j < ntok; ++j) p.logits[static_cast<int64_t>(s_tok[j]) * p.ld + s] = -INFINITY;
+        for (int j = 0; j < ntok; ++j) __stcs(p.logits + static_cast<int64_t>(s_tok[j]) * p.ld + s, -INFINITY);
     }
   }
 
