@@ -13,9 +13,9 @@
 // K = head_dim bytes, 128-byte swizzled), B = the quantised queries of up to
 // four tokens of one request (N = 64 heads x tokens). Each TMEM lane then holds
 // one key, so the ReLU-weighted head sum is an in-thread loop over columns.
-// Key tiles are gathered through the block table with 16-byte cp.async into a
-// ring of shared-memory stages; two CTAs share an SM so one CTA's epilogue
-// overlaps the other's loads and MMAs.
+// Key tiles come through the block table into a ring of shared-memory stages
+// (TMA page loads for 128-dim keys, 16-byte cp.async otherwise); two CTAs
+// share an SM so one CTA's epilogue overlaps the other's loads and MMAs.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -126,9 +126,9 @@ __host__ __device__ inline SmemOffsets indexer_smem(int n_cols, int stages) {
 // two CTAs per SM: stages sized so that 2 x smem stays within 228 KB
 __host__ __device__ inline int indexer_stages(int n_cols) { return n_cols <= 64 ? 6 : (n_cols <= 128 ? 5 : 4); }
 
-// Warp roles: warps 0-3 quantise the queries, then run the epilogue (warp w
-// owns TMEM lanes 32w..32w+31 = keys of the tile); warp 4 loads key tiles
-// (TMA for 128-byte rows, cp.async otherwise); warp 5 issues the MMAs.
+// Warp roles: warps 0-7 quantise the queries, then run the epilogue (warps w
+// and w + 4 read TMEM lanes 32(w%4)..+31 = keys of the tile); warp 8 loads key
+// tiles (TMA for 128-byte rows, cp.async otherwise); warp 9 issues the MMAs.
 template <int DI>
 __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __grid_constant__ IndexerParams p,
                                                                      const __grid_constant__ CUtensorMap kmap) {
@@ -146,6 +146,23 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = blockIdx.y / p.n_tb;
   const int tblk = blockIdx.y % p.n_tb;
+  const int t_begin = blockIdx.x * p.tiles_per_cta;
+  const int t_end = min(t_begin + p.tiles_per_cta, p.n_tiles);
+  // block ids of every key the CTA's tiles can address (warps 8 and 9), read
+  // before the request's length is known; entries past it are never used
+  // because every use first checks the key against seq_len
+  const int* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+  const int blk0 = t_begin * kTileKeys / p.block_size;
+  const int n_blk = max(0, min((t_end * kTileKeys + p.block_size - 1) / p.block_size, p.bt_stride) - blk0);
+  constexpr int kBlkPerThread = (kMaxBlocksPerCta + 63) / 64;
+  int blk_v[kBlkPerThread];
+  if (warp >= 8) {
+#pragma unroll
+    for (int u = 0; u < kBlkPerThread; ++u) {
+      const int i = tid - kEpiThreads + 64 * u;
+      blk_v[u] = i < n_blk ? __ldg(bt_row + blk0 + i) : -1;
+    }
+  }
   const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1);
   const int tok0 = q0 + tblk * p.tb;
   if (tok0 >= q1) return;  // this request has fewer token blocks (uniform exit)
@@ -160,8 +177,6 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   }
   const int max_valid = min(static_cast<int64_t>(seq_len - q_len + (tok0 + ntok - 1 - q0) + 1), cap);
 
-  const int t_begin = blockIdx.x * p.tiles_per_cta;
-  const int t_end = min(t_begin + p.tiles_per_cta, p.n_tiles);
   const int t_comp_end = min(t_end, (max_valid + kTileKeys - 1) / kTileKeys);  // tiles needing an MMA
   const int n_comp = max(0, t_comp_end - t_begin);
   const int n_cols = p.hi_pad * p.tb;  // MMA N
@@ -174,10 +189,6 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   uint8_t* sq = smem + so.q;
   float* sw = reinterpret_cast<float*>(smem + so.w);
 
-  const int* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-  const int blk0 = t_begin * kTileKeys / p.block_size;
-  const int n_blk = n_comp > 0 ? ((t_begin + n_comp) * kTileKeys + p.block_size - 1) / p.block_size - blk0 : 0;
-
   if (tid < ntok) {
     s_tok[tid] = tok0 + tid;
     s_valid[tid] = min(static_cast<int64_t>(seq_len - q_len + (tok0 + tid - q0) + 1), cap);
@@ -187,70 +198,71 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   uint32_t tmem = 0;
   const uint32_t acc_cols = n_cols <= 32 ? 32 : (n_cols <= 64 ? 64 : (n_cols <= 128 ? 128 : 256));
   const uint32_t tmem_cols = acc_cols * nbuf;
-  // ---- prologue. The key loads start as soon as the block ids are known;
-  // warps 0-3 quantise the queries meanwhile (the MMA waits on q_ready).
-  // a0 takes 16 (token, head) rows per pass, 8 lanes per row; the loads of
-  // every pass are issued before the barrier so their latency overlaps it.
-  constexpr int kQPass = 2;  // passes in flight: 64 rows (up to 4 tokens x 16 heads, or 1 token x 64 heads)
-  uint4 qa[kQPass], qb[kQPass];
-  float qw[kQPass];
+  auto abort_now = [&](void) {
+    s_abort = 1;
+    report(p.dev_status, DSA_DEVERR_TIMEOUT);
+  };
+  auto block_ok = [&](int s) {  // key s < seq_len lies in a valid block
+    const int blk = s_blk[s / p.block_size - blk0];
+    return blk >= 0 && blk < p.num_blocks;
+  };
+  // keys that later token blocks of the request read again stay in L2
+  const bool keep_keys = p.n_tb > 1;
+  // tile i: two TMA loads of 64 keys x 128 B (one page each) plus their scales,
+  // completing on full_bar[i % S]; keys past seq_len are neither loaded nor counted
+  auto issue_keys = [&](int i) {
+    const int st = i % S;
+    const int key0 = (t_begin + i) * kTileKeys;
+    uint32_t bytes = 0;
+    int blk_u[2], off_u[2];
+    bool bad = false;
+    for (int u = 0; u < 2; ++u) {
+      const int s0 = key0 + 64 * u;
+      blk_u[u] = -1;
+      off_u[u] = s0 % p.block_size;
+      if (s0 < seq_len) {
+        if (block_ok(s0)) {
+          blk_u[u] = s_blk[s0 / p.block_size - blk0];
+          bytes += 64 * 128 + 64 * 4;
+        } else {
+          bad = true;
+        }
+      }
+    }
+    mbar_arrive_expect_tx(&full_bar[st], bytes);
+    for (int u = 0; u < 2; ++u) {
+      if (blk_u[u] < 0) continue;
+      if (keep_keys)
+        tma_load_3d_hint(smem_u32(sk + st * kTileBytes + u * 8192), &kmap, &full_bar[st], 0, off_u[u], blk_u[u],
+                         l2_policy_evict_last());
+      else
+        tma_load_3d(smem_u32(sk + st * kTileBytes + u * 8192), &kmap, &full_bar[st], 0, off_u[u], blk_u[u]);
+      bulk_copy_g2s(smem_u32(ssc + st * kTileKeys + u * 64),
+                    p.k_cache + static_cast<int64_t>(blk_u[u]) * p.k_block_stride +
+                        static_cast<int64_t>(p.block_size) * 128 + off_u[u] * 4,
+                    256, &full_bar[st]);
+    }
+    if (bad) report(p.dev_status, DSA_DEVERR_BLOCK_OOB);
+  };
+  // tiles whose loads the producer issues before the CTA barrier (TMA path):
+  // one, so that its latency overlaps the prologue; issuing every stage this
+  // early delays the query loads the first MMA also waits for
+  const int n_early = DI == 128 ? min(1, n_comp) : 0;
+
+  // ---- prologue, before one CTA barrier: warps 0-7 load and quantise the
+  // queries (a0) into the B operand; warp 8 stores the block ids, initialises
+  // the barriers and issues the first key tile; warp 9 allocates TMEM.
   if (n_comp > 0) {
     if constexpr (DI < 128) {  // row padding past Di is never written by the loads
       for (int i = tid; i < S * kTileBytes / 16; i += kThreads) reinterpret_cast<uint4*>(sk)[i] = make_uint4(0, 0, 0, 0);
     }
     if (warp < 8) {
-#pragma unroll
-      for (int u = 0; u < kQPass; ++u) {
-        const int n = u * 32 + tid / 8, c = tid % 8;
-        const int j = n / p.hi_pad, h = n % p.hi_pad;
-        qa[u] = make_uint4(0, 0, 0, 0);
-        qb[u] = qa[u];
-        qw[u] = 0.f;
-        if (n < n_cols && j < ntok && h < p.Hi) {
-          if (c < DI / 16) {
-            const uint4* src =
-                reinterpret_cast<const uint4*>(p.q + (tok0 + j) * p.q_stride_t + static_cast<int64_t>(h) * DI) + 2 * c;
-            qa[u] = __ldg(src);
-            qb[u] = __ldg(src + 1);
-          }
-          if (c == 0) qw[u] = __ldg(p.w + static_cast<int64_t>(tok0 + j) * p.Hi + h);
-        }
-      }
-    } else {
-      // block ids of every key this CTA reads (warps 8 and 9)
-      for (int i = tid - kEpiThreads; i < n_blk; i += 64) {
-        const int lb = blk0 + i;
-        s_blk[i] = lb * p.block_size < seq_len ? __ldg(bt_row + lb) : -1;
-      }
-    }
-    if (DI < 128) fence_proxy_async_smem();
-    if (warp == kMmaWarp) {
-      tmem_alloc(&tmem_holder, tmem_cols);
-      tmem_relinquish();
-    }
-    if (tid == 0) {
-      for (int s = 0; s < S; ++s) {
-        mbar_init(&full_bar[s], DI == 128 ? 1 : 32);
-        mbar_init(&empty_bar[s], 1 + 8);
-      }
-      for (int s = 0; s < 2; ++s) {
-        mbar_init(&acc_full[s], 1);
-        mbar_init(&acc_empty[s], 8);
-      }
-      mbar_init(&q_ready, 8);
-      for (int q = 0; q < 4; ++q) mbar_init(&pair_bar[q], 2);  // the two warps of a lane group, once per tile
-      fence_mbar_init();
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (n_comp > 0) tmem = tmem_holder;
-  if (n_comp > 0 && warp < 8) {
-    // a0: the token block's queries -> the B operand (N rows x 128 B) and
-    // the per-column weight w * scale_q
-    for (int base0 = 0; base0 < n_cols; base0 += kQPass * 32) {
-      if (base0 > 0) {  // more than 64 columns: the later passes load here
+      // a0 takes 32 (token, head) rows per pass, 8 lanes per row; the loads of
+      // kQPass passes are in flight together
+      constexpr int kQPass = 2;
+      for (int base0 = 0; base0 < n_cols; base0 += kQPass * 32) {
+        uint4 qa[kQPass], qb[kQPass];
+        float qw[kQPass];
 #pragma unroll
         for (int u = 0; u < kQPass; ++u) {
           const int n = base0 + u * 32 + tid / 8, c = tid % 8;
@@ -268,38 +280,62 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
             if (c == 0) qw[u] = __ldg(p.w + static_cast<int64_t>(tok0 + j) * p.Hi + h);
           }
         }
-      }
 #pragma unroll
-      for (int u = 0; u < kQPass; ++u) {
-        const int n = base0 + u * 32 + tid / 8, c = tid % 8;
-        if (n >= n_cols) break;  // uniform within a warp (n_cols is a multiple of 16)
-        float scale;
-        const uint4 codes = quant_chunk16(qa[u], qb[u], scale);
-        *reinterpret_cast<uint4*>(sq + sw128_offset(n, c)) = codes;
-        if (c == 0) sw[n] = qw[u] * scale;  // zero for padded rows
+        for (int u = 0; u < kQPass; ++u) {
+          const int n = base0 + u * 32 + tid / 8, c = tid % 8;
+          if (n >= n_cols) break;  // uniform within a warp (n_cols is a multiple of 16)
+          float scale;
+          const uint4 codes = quant_chunk16(qa[u], qb[u], scale);
+          *reinterpret_cast<uint4*>(sq + sw128_offset(n, c)) = codes;
+          if (c == 0) sw[n] = qw[u] * scale;  // zero for padded rows
+        }
+      }
+      fence_proxy_async_smem();  // the MMA reads the codes through the async proxy
+    } else {
+#pragma unroll
+      for (int u = 0; u < kBlkPerThread; ++u) {
+        const int i = tid - kEpiThreads + 64 * u;
+        if (i < n_blk) s_blk[i] = blk_v[u];
+      }
+      __syncwarp();
+      if (warp == kProdWarp && lane == 0) {
+        for (int s = 0; s < S; ++s) {
+          mbar_init(&full_bar[s], DI == 128 ? 1 : 32);
+          mbar_init(&empty_bar[s], 1 + 8);
+        }
+        for (int s = 0; s < 2; ++s) {
+          mbar_init(&acc_full[s], 1);
+          mbar_init(&acc_empty[s], 8);
+        }
+        mbar_init(&q_ready, 8);
+        for (int q = 0; q < 4; ++q) mbar_init(&pair_bar[q], 2);  // the two warps of a lane group, once per tile
+        fence_mbar_init();
+        // the tile's block ids were stored by this warp (its first 32 entries
+        // cover the first 16 tiles: block_size >= 64)
+        if constexpr (DI == 128) {
+          for (int i = 0; i < n_early; ++i) issue_keys(i);
+        }
+      }
+      if (warp == kMmaWarp) {
+        tmem_alloc(&tmem_holder, tmem_cols);
+        tmem_relinquish();
       }
     }
-    fence_proxy_async_smem();  // the MMA reads the codes through the async proxy
+    if (DI < 128) fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (n_comp > 0) tmem = tmem_holder;
+  if (n_comp > 0 && warp < 8) {
     __syncwarp();
     if (lane == 0) mbar_arrive(&q_ready);
-    named_barrier_sync(1, kEpiThreads);  // every column weight is written before the epilogue reads them
   }
 
-  auto abort_now = [&](void) {
-    s_abort = 1;
-    report(p.dev_status, DSA_DEVERR_TIMEOUT);
-  };
-  auto block_ok = [&](int s) {  // key s < seq_len lies in a valid block
-    const int blk = s_blk[s / p.block_size - blk0];
-    return blk >= 0 && blk < p.num_blocks;
-  };
 
   if (n_comp > 0 && warp == kProdWarp) {
-    // keys that later token blocks of the request read again stay in L2
-    const bool keep_keys = p.n_tb > 1;
-    const uint64_t l2_keep = l2_policy_evict_last();
-    // ---------------- producer
-    for (int i = 0; i < n_comp && !s_abort; ++i) {
+    // ---------------- producer (the first tile went out before the CTA barrier)
+    for (int i = n_early; i < n_comp && !s_abort; ++i) {
       const int st = i % S;
       if (i >= S && !mbar_wait(&empty_bar[st], ((i / S) - 1) & 1)) {
         if (lane == 0) abort_now();
@@ -307,38 +343,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
       }
       const int key0 = (t_begin + i) * kTileKeys;
       if constexpr (DI == 128) {
-        if (lane == 0) {
-          uint32_t bytes = 0;
-          int blk_u[2], off_u[2];
-          bool bad = false;
-          for (int u = 0; u < 2; ++u) {
-            const int s0 = key0 + 64 * u;
-            blk_u[u] = -1;
-            off_u[u] = s0 % p.block_size;
-            if (s0 < seq_len) {
-              if (block_ok(s0)) {
-                blk_u[u] = s_blk[s0 / p.block_size - blk0];
-                bytes += 64 * 128 + 64 * 4;
-              } else {
-                bad = true;
-              }
-            }
-          }
-          mbar_arrive_expect_tx(&full_bar[st], bytes);
-          for (int u = 0; u < 2; ++u) {
-            if (blk_u[u] < 0) continue;
-            if (keep_keys)
-              tma_load_3d_hint(smem_u32(sk + st * kTileBytes + u * 8192), &kmap, &full_bar[st], 0, off_u[u], blk_u[u],
-                               l2_keep);
-            else
-              tma_load_3d(smem_u32(sk + st * kTileBytes + u * 8192), &kmap, &full_bar[st], 0, off_u[u], blk_u[u]);
-            bulk_copy_g2s(smem_u32(ssc + st * kTileKeys + u * 64),
-                          p.k_cache + static_cast<int64_t>(blk_u[u]) * p.k_block_stride +
-                              static_cast<int64_t>(p.block_size) * 128 + off_u[u] * 4,
-                          256, &full_bar[st]);
-          }
-          if (bad) report(p.dev_status, DSA_DEVERR_BLOCK_OOB);
-        }
+        if (lane == 0) issue_keys(i);
       } else {
         constexpr int kChunks = DI / 16;
         uint8_t* dst_base = sk + st * kTileBytes;
