@@ -196,18 +196,21 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   extern __shared__ uint32_t kc[];  // this part's keys (when cached)
   __shared__ TopkShared sh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // launched as a programmatic dependent of the logits producer: wait for
-  // its results, then let the next kernel's CTAs be scheduled
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int P = p.parts;
   const int r = static_cast<int>(cluster_ctarank());
   const int t = blockIdx.x / P;
   const int k = p.k;
+  // Launched as a programmatic dependent of the logits producer. The row's
+  // valid length comes from the step's inputs, which that kernel does not
+  // write, so it is found first; then wait for the logits and let the next
+  // kernel's CTAs be scheduled.
+  const int n = valid_length(p.seq_lens, p.qsl, p.B, t, p.ld, sh);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int32_t* out = p.out + static_cast<int64_t>(t) * k;
   const float* row = p.logits + static_cast<int64_t>(t) * p.ld;
-  // The row's parts are cut by ld, so the first values are loaded before
-  // valid(t) is known; positions at or past valid(t) are ignored afterwards.
+  // The row's parts are cut by ld, so the first values are loaded whatever
+  // valid(t) is; positions at or past valid(t) are ignored afterwards.
   const int ld = static_cast<int>(p.ld);
   const int seg = (ld + P - 1) / P;
   const int s0 = min(ld, r * seg);
@@ -218,7 +221,6 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     const int i = u * kThreads + tid;
     v_first[u] = i < m_ld ? __ldg(row + s0 + i) : 0.f;
   }
-  const int n = valid_length(p.seq_lens, p.qsl, p.B, t, p.ld, sh);
   if (n <= k) {  // every valid position, then -1 (the same branch for the whole cluster)
     const int o0 = static_cast<int>(static_cast<int64_t>(r) * k / P);
     const int o1 = static_cast<int>(static_cast<int64_t>(r + 1) * k / P);
@@ -484,22 +486,24 @@ template <int VPT>
 __global__ void __launch_bounds__(kThreads) topk_row_kernel(const TopkParams p) {
   __shared__ TopkShared sh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int t = blockIdx.x;
   const int k = p.k;
+  // the row's valid length comes from the step's inputs, which the logits
+  // producer does not write: it is found while that kernel may still run
+  const int n = valid_length(p.seq_lens, p.qsl, p.B, t, p.ld, sh);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int32_t* out = p.out + static_cast<int64_t>(t) * k;
+  if (n <= k) {
+    for (int i = tid; i < k; i += kThreads) out[i] = i < n ? i : -1;
+    return;
+  }
   const float* row = p.logits + static_cast<int64_t>(t) * p.ld;
   const int ld = static_cast<int>(p.ld);
   const int base = warp * 32 * VPT + lane;  // position of key[0]; key[u] sits at base + 32 u
   uint32_t key[VPT];
 #pragma unroll
   for (int u = 0; u < VPT; ++u) key[u] = base + 32 * u < ld ? order_key(__ldg(row + base + 32 * u)) : 0u;
-  const int n = valid_length(p.seq_lens, p.qsl, p.B, t, p.ld, sh);
-  if (n <= k) {
-    for (int i = tid; i < k; i += kThreads) out[i] = i < n ? i : -1;
-    return;
-  }
   auto valid = [&](int u) { return base + 32 * u < n; };
 
   // ---- exact finite range of the row; histogram over 2048 bins linear in it

@@ -210,3 +210,32 @@ def test_bad_block_ids_are_masked_and_reported():
     lg = step.logits.cpu().numpy()
     assert np.all(np.isneginf(lg[0, 128:192]))  # keys of the bad block
     assert np.all(np.isfinite(lg[0, :128]))
+
+
+def test_unused_block_table_entries_are_ignored():
+    """Entries of a request's block-table row past its length may hold anything:
+    the kernels may read them but never use them, so results are unchanged and
+    no error is reported."""
+    wl = _wl("decode_small")
+    step = DsaStep(wl)
+    step.run()
+    torch.cuda.synchronize()
+    ref = (step.logits.clone(), step.topk_idx.clone(), step.out.clone())
+    bt = step.block_table.cpu().numpy().copy()
+    garbage = np.array([wl.num_blocks + 7, 0, wl.num_blocks - 1, 2**30, -5], dtype=np.int32)
+    touched = 0
+    for b in range(bt.shape[0]):
+        used = -(-int(wl.seq_lens[b]) // wl.block_size)
+        n = bt.shape[1] - used
+        bt[b, used:] = np.resize(garbage, n)
+        touched += n
+    assert touched > 0
+    step.block_table.copy_(torch.from_numpy(bt))
+    step.dev_status.zero_()
+    step.logits.fill_(float("nan"))
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) == 0
+    assert torch.equal(step.logits, ref[0])
+    assert torch.equal(step.topk_idx, ref[1])
+    assert torch.equal(step.out, ref[2])
