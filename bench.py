@@ -20,6 +20,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -51,7 +52,8 @@ def dist_info():
 
 
 def algorithmic_bytes(wl, topk_idx_host=None):
-    """Bytes each kernel must move at minimum (the design doc lists the formulas)."""
+    """Bytes each kernel must move at minimum: its inputs read once, its outputs
+    written once (gathered rows counted once per selected valid slot)."""
     T, ld, K = wl.T, wl.ld, wl.index_topk
     qsl = wl.query_start_loc
     valid = []
@@ -93,7 +95,8 @@ class ClockSampler:
         self.path = None
 
     def start(self):
-        out_dir = os.path.join(ROOT, "gpurun_out")
+        # the raw samples go to DSA_BENCH_OUT (default: the system temp directory)
+        out_dir = os.environ.get("DSA_BENCH_OUT") or tempfile.gettempdir()
         os.makedirs(out_dir, exist_ok=True)
         self.path = os.path.join(out_dir, f"clocks_rank{self.gpu}.csv")
         try:

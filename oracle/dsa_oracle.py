@@ -30,7 +30,7 @@ Sources (web pages; cited by title and section):
   The step's formulas: logits[t,s] = sum_h w[t,h] * ReLU(q[t,h,:] . dequant(k[s,:]));
   top-k of each logits row; softmax attention over the selected rows.
 
-Readings where the pages are silent (each one is listed in the design doc):
+Readings where the pages are silent:
   * e4m3 is OCP E4M3FN: bias 7, max 448, no infinities, S.1111.111 is NaN.
   * q quantisation: per (token, head) group of head_dim values,
     scale = amax / 448 in fp32; codes = e4m3_rn_sat(fp32(x / scale)); amax == 0
