@@ -14,6 +14,8 @@ float64 with numpy, one query token at a time:
   a3  sparse MLA attention over the selected rows of a paged bf16 latent cache,
       single pass or split into KV splits
   a4  merge of the split partials by online softmax
+  and, on the producer side, the new tokens' indexer keys quantised into the
+  paged fp8 key cache (indexer_k_quant_and_cache)
 
 Sources (web pages; cited by title and section):
   [PR]     vLLM PR #38476, "[Feature] TRITON_MLA_SPARSE backend for SM8x/11x/12x
@@ -37,6 +39,8 @@ Readings where the pages are silent:
     gives scale 1 and all-zero codes.
   * Indexer page layout inside one block of block_size tokens: block_size x 128
     e4m3 bytes (token-major) followed by block_size fp32 scales.
+  * The new tokens' keys are quantised with the q rule (one group = a key's Di
+    values) and stored at the tokens' own positions (below).
   * seq_lens include the new tokens, whose keys are already in the cache;
     query token t of request b sits at position seq_len_b - q_len_b + (t - qsl_b)
     and sees keys s <= that position.
@@ -176,6 +180,39 @@ def token_positions(seq_lens, query_start_loc):
             req[t] = b
             pos[t] = seq_lens[b] - q_len + i
     return req, pos
+
+
+def indexer_k_quant_and_cache(k, k_cache, k_block_stride, block_table, seq_lens, query_start_loc, block_size):
+    """Producer side of the indexer key cache: a copy of k_cache with the T
+    new tokens' keys stored.
+
+    [README] "The skew fixes" item 0 names indexer_k_quant_and_cache as the op
+    that writes the indexer page (block_size rows of Di e4m3 bytes, then
+    block_size fp32 scales) and addresses blocks through the cache's block
+    stride. Each key row k[t] (bf16 values, exact in fp32) is quantised with
+    the a0 rule of quantize_groups; token t of request b lands at position
+    pos(t) of token_positions: block block_table[b, pos // block_size], row
+    pos % block_size. A position past the block-table row or a block id
+    outside the cache skips the token (the device code reports it).
+    """
+    k = np.asarray(k, dtype=np.float32)
+    T, Di = k.shape
+    codes, scales = quantize_groups(k)
+    out = np.array(k_cache, dtype=np.uint8, copy=True).reshape(-1, k_block_stride)
+    bt = np.asarray(block_table)
+    req, pos = token_positions(seq_lens, query_start_loc)
+    for t in range(T):
+        b, p = int(req[t]), int(pos[t])
+        if p < 0 or p >= bt.shape[1] * block_size:
+            continue
+        blk = int(bt[b, p // block_size])
+        if blk < 0 or blk >= out.shape[0]:
+            continue
+        off = p % block_size
+        out[blk, off * Di:(off + 1) * Di] = codes[t]
+        sc0 = block_size * Di + off * 4
+        out[blk, sc0:sc0 + 4] = np.array([scales[t]], dtype=np.float32).view(np.uint8)
+    return out.reshape(np.shape(k_cache))
 
 
 def gather_index_keys(k_cache: np.ndarray, block_stride: int, block_table_row, n_keys: int, block_size: int, head_dim: int):

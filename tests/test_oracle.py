@@ -230,6 +230,61 @@ def test_indexer_paging_is_transparent():
     assert np.array_equal(o1, o2)
 
 
+# ------------------------------------------------- producer: key cache writes
+def test_k_quant_and_cache_worked_example():
+    """Request of 130 keys whose last 3 are new; block size 64, table [4, 0, 2]:
+    positions 127, 128, 129 -> block 0 row 63, block 2 rows 0 and 1."""
+    bs, Di = 64, 128
+    stride = bs * (Di + 4)
+    cache = np.full((5, stride), 0xA5, dtype=np.uint8)
+    k = np.random.default_rng(3).standard_normal((3, Di)).astype(np.float32)
+    out = O.indexer_k_quant_and_cache(k, cache, stride, np.array([[4, 0, 2]]), np.array([130]), np.array([0, 3]), bs)
+    codes, scales = O.quantize_groups(k)
+    want = cache.copy()
+    for (blk, row), t in (((0, 63), 0), ((2, 0), 1), ((2, 1), 2)):
+        want[blk, row * Di:(row + 1) * Di] = codes[t]
+        want[blk, bs * Di + 4 * row: bs * Di + 4 * row + 4] = np.frombuffer(np.float32(scales[t]).tobytes(), np.uint8)
+    assert np.array_equal(out, want)
+    assert np.array_equal(out[[1, 3, 4]], cache[[1, 3, 4]])  # other blocks untouched
+
+
+def test_k_quant_and_cache_fills_the_page_the_indexer_reads():
+    """Writing every key of two prompts (seq_len == q_len) gives the cache the
+    test's own packer lays out by key index, so the indexer reads them back."""
+    rng = np.random.default_rng(11)
+    bs, Di = 4, 8
+    lens = [9, 6]
+    tables = [[3, 0, 5], [1, 4]]
+    keys = [rng.standard_normal((n, Di)).astype(np.float32) for n in lens]
+    stride = bs * (Di + 4)
+    bt = np.full((2, 3), -1, dtype=np.int32)
+    for b, tb in enumerate(tables):
+        bt[b, :len(tb)] = tb
+    qsl = np.array([0, lens[0], lens[0] + lens[1]])
+    out = O.indexer_k_quant_and_cache(np.concatenate(keys), np.zeros((6, stride), np.uint8), stride, bt, np.array(lens),
+                                      qsl, bs)
+    want = np.zeros((6, stride), np.uint8)
+    for b in range(2):
+        kc, ks = O.quantize_groups(keys[b])
+        packed, _ = _pack_index_cache(kc, ks, bs, Di, tables[b])
+        used = sorted(set(tables[b]))
+        want[used] = packed[used]
+    assert np.array_equal(out, want)
+
+
+def test_k_quant_matches_the_torch_cast_recipe():
+    """The key rule: scale = fp32(amax / 448) and codes = e4m3fn cast of
+    fp32(x / scale), the recipe of PyTorch's own float8 cast."""
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((256, 128)) * rng.uniform(1e-3, 1e3, (256, 1))).astype(np.float32)
+    codes, scales = O.quantize_groups(x)
+    amax = np.abs(x).max(axis=1)
+    s_ref = (amax / np.float32(448.0)).astype(np.float32)
+    c_ref = torch.from_numpy((x / s_ref[:, None]).astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(scales, s_ref)
+    assert np.array_equal(codes, c_ref)
+
+
 # --------------------------------------------------------------------- a2
 def test_topk_hand_example():
     g = GOLDEN["topk"]
