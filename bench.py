@@ -275,6 +275,23 @@ def main():
     t_idx = [evb[k][0].elapsed_time(evb[k][1]) for k in range(Kb)]
     t_topk = [evb[k][2].elapsed_time(evb[k][3]) for k in range(Kb)]
     t_att = [evb[k][4].elapsed_time(evb[k][5]) for k in range(Kb)]
+    # producer side, not part of the step: the new tokens' indexer keys
+    # quantised into a scratch copy of the key cache
+    from deepseek_sparse_attention_fp8_gb300 import api
+
+    gen = torch.Generator(device=step.device).manual_seed(1234)
+    k_new = torch.randn((wl.T, wl.Di), generator=gen, device=step.device).to(torch.bfloat16)
+    k_scratch = step.k_cache.clone()
+    evp = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kb)]
+    for k in range(Kb):
+        flush_l2()
+        evp[k][0].record(stream)
+        api.dsa_indexer_k_quant_and_cache(k_new, k_scratch, step.block_table, step.seq_lens, step.qsl, wl.block_size,
+                                          dev_status=step.dev_status)
+        evp[k][1].record(stream)
+    barrier()
+    t_prod = [evp[k][0].elapsed_time(evp[k][1]) for k in range(Kb)]
+    del k_scratch
     from deepseek_sparse_attention_fp8_gb300.replicas import aggregate
 
     ms, _, value = aggregate(float(np.mean(t_step)), wl.T, step.device)
@@ -327,6 +344,11 @@ def main():
     for k_, v in kern.items():
         v["GBps"] = v["bytes"] / (v["ms"] / 1e3) / 1e9
         v["frac"] = v["GBps"] / peak
+    # bf16 keys read, codes and scales written
+    prod_bytes = wl.T * (wl.Di * 2 + wl.Di + 4)
+    producer = {"indexer_k_quant_and_cache": {"ms": float(np.mean(t_prod)), "bytes": prod_bytes,
+                                              "GBps": prod_bytes / (float(np.mean(t_prod)) / 1e3) / 1e9}}
+    producer["indexer_k_quant_and_cache"]["frac"] = producer["indexer_k_quant_and_cache"]["GBps"] / peak
     dom = max(kern, key=lambda k_: kern[k_]["ms"])
     traffic = load_traffic(dom, wl.name)
     step_bytes = alg["indexer"] + alg["topk"] + alg["attention"]
@@ -343,6 +365,7 @@ def main():
                      "frac": kern[dom]["frac"], "peak_source": peak_kind, "traffic": traffic,
                      "step_GBps": step_bytes / (ms / 1e3) / 1e9, "step_frac": step_bytes / (ms / 1e3) / 1e9 / peak},
         "kernels": kern,
+        "producer": producer,
         "warm_l2_ms_per_step": ms_warm,
         "gpu_launches": step.kernel_launches() * K,
         "clocks": clocks,

@@ -37,6 +37,8 @@ _SIGS = {
     "dsa_quant_q": ([_p, _i64, _i32, _i32, _i32, _p, _p, _p], _i32),
     "dsa_indexer_logits": ([_p, _i64, _p, _p, _i64, _i32, _p, _i32, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _p,
                             _i64, _p, _p], _i32),
+    "dsa_indexer_k_quant_and_cache": ([_p, _i64, _i32, _i32, _p, _i64, _i32, _p, _i32, _p, _p, _i32, _i32, _p, _p],
+                                      _i32),
     "dsa_topk_workspace_size": ([_i32, _i64, _i32], _sz),
     "dsa_topk": ([_p, _i64, _p, _p, _i32, _i32, _i32, _p, _p, _sz, _p], _i32),
     "sparse_mla_workspace_size": ([_i32, _i32, _i32, _i32], _sz),
@@ -102,6 +104,27 @@ def dsa_quant_q(q_idx, q8=None, sq=None, stream=None):
     _need(sq, torch.float32, "sq", 2)
     _check(lib.dsa_quant_q(_ptr(q_idx), Hi * Di, T, Hi, Di, _ptr(q8), _ptr(sq), _stream(stream)), "dsa_quant_q")
     return q8, sq
+
+
+def dsa_indexer_k_quant_and_cache(k, k_cache, block_table, seq_lens, query_start_loc, block_size, dev_status=None,
+                                  stream=None):
+    """Quantises the new tokens' indexer keys k [T, Di] (bf16) to e4m3 with one
+    fp32 scale per token and stores them into the paged fp8 key cache
+    k_cache [num_blocks, k_block_stride_bytes] (uint8) in place."""
+    _need(k, torch.bfloat16, "k", 2)
+    _need(k_cache, torch.uint8, "k_cache", 2)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(query_start_loc, torch.int32, "query_start_loc", 1)
+    if dev_status is not None:
+        _need(dev_status, torch.int32, "dev_status")
+    T, Di = k.shape
+    st = lib.dsa_indexer_k_quant_and_cache(_ptr(k), Di, T, Di, _ptr(k_cache), k_cache.shape[1], k_cache.shape[0],
+                                           _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                           _ptr(query_start_loc), seq_lens.shape[0], block_size, _ptr(dev_status),
+                                           _stream(stream))
+    _check(st, "dsa_indexer_k_quant_and_cache")
+    return k_cache
 
 
 def dsa_indexer_logits(q_idx, w, k_cache, block_table, seq_lens, query_start_loc, block_size, max_q_len, logits,

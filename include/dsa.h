@@ -118,6 +118,32 @@ dsa_status_t dsa_indexer_logits(const void* q_idx, int64_t q_stride_t, const flo
                                 float* logits, int64_t ld, int32_t* dev_status, dsa_stream_t stream);
 
 /*
+ * Producer side of the indexer key cache (the op indexer_k_quant_and_cache
+ * of the "vllm-dsa-mtp-sm80" README, "The skew fixes", item 0): quantise the
+ * keys of the T new query tokens and store them in the paged fp8 cache that
+ * dsa_indexer_logits reads.
+ *   k        bf16 [T, Di], token stride k_stride_t elements (>= Di, a multiple
+ *            of 8; 16-byte aligned), one row per query token in query order
+ *   k_cache  the indexer key cache (layout above), written in place: for each
+ *            token t of request b, the Di code bytes and the fp32 scale of key
+ *            position pos(t) = seq_lens[b] - q_len_b + (t - query_start_loc[b])
+ *            in block block_table[b, pos(t) / block_size]. Nothing else of the
+ *            cache is touched.
+ * Per token: scale = amax(|k[t,:]|)/448 (1 when amax == 0) and code =
+ * e4m3_rn_satfinite(k / scale), both divisions IEEE-rounded fp32: the rule of
+ * a0 applied to the key row (finite inputs). A position outside the block
+ * table (DSA_DEVERR_SEQ_LEN) or a block id outside [0, num_blocks)
+ * (DSA_DEVERR_BLOCK_OOB) skips that token. Supported: Di in {32, 64, 128};
+ * block_size a multiple of 64. Tokens must not share a position (each writes
+ * its row without ordering against the others).
+ */
+dsa_status_t dsa_indexer_k_quant_and_cache(const void* k, int64_t k_stride_t, int32_t T, int32_t Di, uint8_t* k_cache,
+                                           int64_t k_block_stride_bytes, int32_t num_blocks,
+                                           const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                           const int32_t* query_start_loc, int32_t B, int32_t block_size,
+                                           int32_t* dev_status, dsa_stream_t stream);
+
+/*
  * a2: top-k of each logits row.
  * Row t ranks logits[t, 0:valid(t)] (fp32, compared as floats so -0.0 equals
  * +0.0); the n = min(index_topk, valid(t)) largest are selected, equal values

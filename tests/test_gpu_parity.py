@@ -239,3 +239,83 @@ def test_unused_block_table_entries_are_ignored():
     assert torch.equal(step.logits, ref[0])
     assert torch.equal(step.topk_idx, ref[1])
     assert torch.equal(step.out, ref[2])
+
+
+def _k_cache_case(Di, bs, seq, q_lens, seed):
+    """A small paged key cache of random bytes (so untouched bytes are checked
+    too), a permuted block table and new keys of varied magnitudes."""
+    rng = np.random.default_rng(seed)
+    B, T = len(seq), sum(q_lens)
+    qsl = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    nblk = [max(1, -(-s // bs)) for s in seq]
+    num_blocks = sum(nblk) + 5
+    phys = rng.permutation(num_blocks).astype(np.int32)
+    bt = np.full((B, max(nblk) + 1), -1, dtype=np.int32)
+    cur = 0
+    for b, n in enumerate(nblk):
+        bt[b, :n] = phys[cur:cur + n]
+        cur += n
+    stride = bs * (Di + 4) + 16  # a padded page: bytes past the layout stay as they were
+    cache = rng.integers(0, 256, (num_blocks, stride), dtype=np.uint8)
+    kf = (rng.standard_normal((T, Di)) * rng.uniform(1e-2, 1e2, (T, 1))).astype(np.float32)
+    kf[min(2, T - 1)] = 0.0  # amax == 0: scale 1, codes 0
+    k = torch.from_numpy(kf).to(torch.bfloat16)
+    return dict(k=k, cache=cache, bt=bt, seq=np.array(seq, dtype=np.int32), qsl=qsl, stride=stride)
+
+
+def _run_k_cache(c, bs):
+    dev = torch.device("cuda")
+    cache = torch.from_numpy(c["cache"]).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    api.dsa_indexer_k_quant_and_cache(c["k"].to(dev), cache, torch.from_numpy(c["bt"]).to(dev),
+                                      torch.from_numpy(c["seq"]).to(dev), torch.from_numpy(c["qsl"]).to(dev), bs,
+                                      dev_status=status)
+    torch.cuda.synchronize()
+    want = O.indexer_k_quant_and_cache(c["k"].float().numpy(), c["cache"], c["stride"], c["bt"], c["seq"], c["qsl"], bs)
+    return cache.cpu().numpy(), want, int(status.item())
+
+
+@pytest.mark.parametrize("Di,bs", [(128, 64), (64, 128), (32, 64)])
+def test_k_quant_and_cache_bit_exact(Di, bs):
+    # decode, MTP pair, a 5-token chunk, and a request made of new tokens only
+    c = _k_cache_case(Di, bs, seq=[70, 129, 200, 3], q_lens=[1, 2, 5, 3], seed=21 + Di)
+    got, want, st = _run_k_cache(c, bs)
+    assert st == 0
+    assert np.array_equal(got, want)
+
+
+def test_k_quant_and_cache_skips_and_reports_bad_targets():
+    bs = 64
+    c = _k_cache_case(128, bs, seq=[70, 129, 1], q_lens=[1, 2, 2], seed=5)
+    c["bt"][1, 127 // bs] = int(c["bt"].max()) + 1000  # request 1's first new key -> block outside the cache
+    got, want, st = _run_k_cache(c, bs)
+    # request 2 has seq_len 1 < q_len 2: its first token has no position
+    assert st & api.DSA_DEVERR_BLOCK_OOB and st & api.DSA_DEVERR_SEQ_LEN
+    assert np.array_equal(got, want)  # the oracle skips the same tokens
+
+
+def test_batch_invariance_with_fixed_splits():
+    """With the split count fixed, a request's logits, top-k and attention
+    output do not depend on which other requests share the batch (every
+    kernel works on one token or one token block at a time)."""
+    import dataclasses
+
+    wl = _wl("mtp2_small")
+    full = DsaStep(wl, num_kv_splits=2)
+    full.run()
+    torch.cuda.synchronize()
+    qsl = wl.query_start_loc
+    for b in (1, 3):
+        t0, t1 = int(qsl[b]), int(qsl[b + 1])
+        sub = dataclasses.replace(wl, B=1, T=t1 - t0, seq_lens=wl.seq_lens[b:b + 1].copy(),
+                                  query_start_loc=np.array([0, t1 - t0], dtype=np.int32),
+                                  block_table=wl.block_table[b:b + 1].copy(), q_idx=wl.q_idx[t0:t1].copy(),
+                                  w=wl.w[t0:t1].copy(), q=wl.q[t0:t1].copy())
+        one = DsaStep(sub, num_kv_splits=2)
+        one.run()
+        torch.cuda.synchronize()
+        assert int(one.dev_status.item()) == 0
+        assert torch.equal(one.logits, full.logits[t0:t1])
+        assert torch.equal(one.topk_idx, full.topk_idx[t0:t1])
+        assert torch.equal(one.out, full.out[t0:t1])
+        assert torch.equal(one.lse, full.lse[t0:t1])

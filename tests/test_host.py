@@ -95,3 +95,21 @@ def test_mla_rejects_bad_arguments(api):
     null_q = [_null()] + base[1:]
     assert lib.sparse_mla_prefill(*null_q, 576, 512, 2048, 64, 0.04, fake, _null(), _null(), _null()) == \
         api.DSA_ERR_INVALID_ARG
+
+
+def test_k_quant_and_cache_rejects_bad_arguments(api):
+    lib = api.lib
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+
+    def call(T=4, Di=128, bs=64, stride=64 * 132, k_stride=128, k=fake):
+        return lib.dsa_indexer_k_quant_and_cache(k, k_stride, T, Di, fake, stride, 10, fake, 4, fake, fake, 1, bs,
+                                                 _null(), _null())
+
+    assert call(Di=48) == api.DSA_ERR_UNSUPPORTED
+    assert call(bs=32) == api.DSA_ERR_UNSUPPORTED
+    assert call(stride=64 * 132 - 16) == api.DSA_ERR_INVALID_ARG
+    assert call(k_stride=100) == api.DSA_ERR_INVALID_ARG
+    assert call(k=_null()) == api.DSA_ERR_INVALID_ARG
+    assert b"null" in lib.dsa_last_error()
+    assert call(T=-1) == api.DSA_ERR_INVALID_ARG
+    assert call(T=0) == api.DSA_OK  # nothing to do: no device touched
