@@ -8,10 +8,11 @@
 //   out = sum_i softmax(s)_i * kv[i, :Dv]     lse = log sum_i exp(s_i)
 //
 // The 128 heads are the MMA M dimension. For Dk = 576 a (token, split) is
-// one 2-CTA cluster: CTA r owns K-blocks (64 dims each) [0,4) or [4,9) of
-// every row, gathers only those (4-row TMA gathers through the block table;
+// one 2-CTA cluster: CTA r owns K-blocks (64 dims each) [4r, 4r+4) and half
+// of the rope dims, [512+32r, 544+32r), of every row, gathers only those
+// (4-row TMA gathers through the block table, 576 bytes of each row per CTA;
 // empty or invalid slots read as zeros and score the sentinel with weight 0),
-// and owns value dims [256r, 256r+256), which are its first four K-blocks.
+// and owns value dims [256r, 256r+256), which are its four K-blocks.
 // Per 64-key tile, in each CTA:
 //   S_r = Q_r K_r^T   tcgen05 kind::f16, M=128, N=64, A (this CTA's q dims)
 //                     in tensor memory, B from the swizzled KV stage;

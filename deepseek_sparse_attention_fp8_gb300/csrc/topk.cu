@@ -8,7 +8,10 @@
 // therefore the exact top-k set with ties resolved toward the lower
 // position, listed in ascending position.
 //
-// A row is cut into P contiguous parts (P = 1..8), one CTA each, the P CTAs
+// Rows of at most 32768 keys, when one CTA per row already fills the GPU,
+// take topk_row_kernel: one CTA holds the whole row in registers (each warp a
+// contiguous run), so the steps below need no staging and no cluster.
+// Otherwise a row is cut into P contiguous parts (P = 1..8), one CTA each, the P CTAs
 // of a row forming a thread-block cluster that combines its histograms and
 // counts through distributed shared memory:
 //   1. each CTA stages its part's keys in shared memory and finds the part's
@@ -20,7 +23,7 @@
 //   3. T is the exact rank selection among that bin's elements (tens, for
 //      logits of a smooth distribution, gathered into every CTA), whose
 //      positions and the parts' counts above the bin also give each part's
-//      output offset. A bin of more than 512 elements is refined instead by
+//      output offset. A bin of more than 1024 elements is refined instead by
 //      histograms over its key interval, each level shrinking the interval
 //      2048-fold, until it holds one key; the parts then exchange counts;
 //   4. an ordered compaction writes each part's selected positions.
