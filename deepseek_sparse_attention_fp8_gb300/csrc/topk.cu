@@ -45,6 +45,8 @@ constexpr int kMaxParts = 8;     // CTAs per row (portable cluster size)
 constexpr int kSegCap = 32768;   // keys of one part staged in shared memory
 constexpr int kBins = 2048;      // histogram bins
 constexpr int kCandCap = kThreads;  // threshold-bin elements ranked directly (one per thread)
+constexpr int kListCap = 512;       // candidate positions one warp may record (cached cluster kernel)
+constexpr int kFilterRatio = 8;     // rows with valid >= 8 k record candidates above a sampled bin
 
 struct TopkShared {
   uint32_t hist[kBins];   // this CTA's histogram (read by the peers)
@@ -61,7 +63,8 @@ struct TopkShared {
   uint64_t scan[kWarps];
   float red_f[2][kWarps];
   uint32_t red_u[3][kWarps];
-  uint32_t bsel, above, thr;
+  uint32_t part_ovf[1];              // a warp's candidate list overflowed in this part
+  uint32_t bsel, above, thr, gtotal;
   int32_t qsl_s[kThreads + 1], sl_s[kThreads];  // the batch's query_start_loc and seq_lens (B <= kThreads)
 };
 
@@ -161,7 +164,7 @@ __device__ int valid_length(const int32_t* seq_lens, const int32_t* qsl, int B, 
 
 // The bin of the row histogram `ghist` holding the `need`-th largest element
 // (bins scanned from the top): sets sh.bsel and sh.above (elements in higher
-// bins). Requires 1 <= need <= the histogram's total.
+// bins) when 1 <= need <= the histogram's total, which goes to sh.gtotal.
 __device__ void find_bin(TopkShared& sh, uint32_t need) {
   const int tid = threadIdx.x;
   constexpr int kPer = kBins / kThreads;  // bins per thread, descending
@@ -181,6 +184,7 @@ __device__ void find_bin(TopkShared& sh, uint32_t need) {
     }
     before += h[u];
   }
+  if (tid == 0) sh.gtotal = static_cast<uint32_t>(tot);
   __syncthreads();
 }
 
@@ -218,11 +222,16 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   const int seg = (ld + P - 1) / P;
   const int s0 = min(ld, r * seg);
   const int m_ld = min(ld, s0 + seg) - s0;
-  float v_first[8];
+  const int m = max(0, min(n - s0, m_ld));  // this part's valid length (may be 0)
+  // warp w stages (and later compacts) the contiguous run [w0, w1) of the part
+  const int wrun = (((m + kWarps - 1) / kWarps) + 31) & ~31;
+  const int w0 = min(m, warp * wrun), w1 = min(m, w0 + wrun);
+  constexpr int kFirst = 4;  // values loaded before the samples, overlapping their latency
+  float v_first[kFirst];
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int i = u * kThreads + tid;
-    v_first[u] = i < m_ld ? __ldg(row + s0 + i) : 0.f;
+  for (int u = 0; u < kFirst; ++u) {
+    const int i = w0 + 32 * u + lane;
+    v_first[u] = i < w1 ? __ldg(row + s0 + i) : 0.f;
   }
   if (n <= k) {  // every valid position, then -1 (the same branch for the whole cluster)
     const int o0 = static_cast<int>(static_cast<int64_t>(r) * k / P);
@@ -230,7 +239,12 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     for (int i = o0 + tid; i < o1; i += kThreads) out[i] = i < n ? i : -1;
     return;
   }
-  const int m = max(0, min(n - s0, m_ld));  // this part's valid length (may be 0)
+  // Rows that keep a small fraction of their keys record, per warp and in
+  // position order, the positions whose bin is at least a bin taken from the
+  // row's samples (a 1.25x margin on k/valid); the later passes then visit
+  // those candidates only. The same in every CTA of the row.
+  const bool use_filter = kCached && static_cast<int64_t>(n) >= static_cast<int64_t>(kFilterRatio) * k;
+  uint16_t* lst = reinterpret_cast<uint16_t*>(kc + ((seg + 7) & ~7)) + warp * kListCap;  // this warp's list
   auto key_at = [&](int i) -> uint32_t {
     if constexpr (kCached) return kc[i];
     else return order_key(__ldg(row + s0 + i));
@@ -250,18 +264,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     sh.loc_n = 0u;
   }
   float lo = INFINITY, hi = -INFINITY;
+  const int ns = min(n, 1024);
+  static_assert(kThreads == 1024, "one sample per thread");
+  const float v_smp = tid < ns ? __ldg(row + static_cast<int64_t>(tid) * n / ns) : 0.f;
   {
-    const int ns = min(n, 1024);
-#pragma unroll
-    for (int u = 0; u < 1024 / kThreads; ++u) {
-      const int j = u * kThreads + tid;
-      if (j < ns) {
-        const float v = __ldg(row + static_cast<int64_t>(j) * n / ns);
-        if (isfinite(v)) {
-          lo = fminf(lo, v);
-          hi = fmaxf(hi, v);
-        }
-      }
+    if (tid < ns && isfinite(v_smp)) {
+      lo = v_smp;
+      hi = v_smp;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -284,26 +293,51 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   float inv_w = hi > lo ? static_cast<float>(kBins) / (hi - lo) : 0.f;
   if (!isfinite(inv_w)) inv_w = 0.f;
   if (!(lo <= hi)) lo = 0.f;
+  int b_tau = 0;  // candidates: bin >= b_tau
+  if (use_filter) {
+    for (int b = tid; b < kBins; b += kThreads) sh.ghist[b] = 0u;
+    __syncthreads();
+    if (tid < ns) atomicAdd(&sh.ghist[lin_bin(key_value(order_key(v_smp)), lo, inv_w)], 1u);
+    __syncthreads();
+    const int64_t want = (static_cast<int64_t>(ns) * k * 5 + static_cast<int64_t>(n) * 4 - 1) / (static_cast<int64_t>(n) * 4) + 8;
+    find_bin(sh, static_cast<uint32_t>(want < ns ? want : static_cast<int64_t>(ns)));
+    b_tau = static_cast<int>(sh.bsel);
+  }
 
   // ---- 2. stage the keys and count them into the part's histogram; CTA r
   // then sums its slice of bins over the cluster and writes the sums into
   // every CTA
-  for (int base = 0; base < m; base += 8 * kThreads) {
+  const uint32_t lt = (1u << lane) - 1u;
+  int cnt_w = 0;  // candidates this warp saw (the list keeps the first kListCap)
+  for (int base = w0; base < w1; base += 8 * 32) {
     float v[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int i = base + u * kThreads + tid;
-      v[u] = base == 0 ? v_first[u] : (i < m ? __ldg(row + s0 + i) : 0.f);
+      const int i = base + 32 * u + lane;
+      v[u] = (base == w0 && u < kFirst) ? v_first[u < kFirst ? u : 0] : (i < w1 ? __ldg(row + s0 + i) : 0.f);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int i = base + u * kThreads + tid;
-      if (i < m) {
-        const uint32_t key = order_key(v[u]);
-        if constexpr (kCached) kc[i] = key;
-        atomicAdd(&sh.hist[lin_bin(key_value(key), lo, inv_w)], 1u);
+      const int i = base + 32 * u + lane;
+      const bool ok = i < w1;
+      const uint32_t key = order_key(v[u]);
+      const int b = lin_bin(key_value(key), lo, inv_w);
+      if constexpr (kCached) {
+        if (ok) kc[i] = key;
+      }
+      const bool cand = ok && b >= b_tau;  // every valid key when there is no filter
+      if (cand) atomicAdd(&sh.hist[b], 1u);
+      if (use_filter) {
+        const uint32_t msk = __ballot_sync(0xFFFFFFFFu, cand);
+        const int slot = cnt_w + __popc(msk & lt);
+        if (cand && slot < kListCap) lst[slot] = static_cast<uint16_t>(i);
+        cnt_w += __popc(msk);
       }
     }
+  }
+  if (use_filter) {  // this part's flag, read by the row's CTAs after the next cluster barrier
+    const int ovf = __syncthreads_or(cnt_w > kListCap);
+    if (tid == 0) sh.part_ovf[0] = static_cast<uint32_t>(ovf);
   }
   const int sl0 = r * (kBins / P), sl1 = (r + 1) * (kBins / P);
   auto reduce_hist = [&]() {
@@ -317,6 +351,24 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   };
   reduce_hist();
   find_bin(sh, static_cast<uint32_t>(k));
+  // the candidate lists serve when the row's candidates hold the top k and
+  // no warp's list overflowed; otherwise the passes below visit every key
+  bool fast = false;
+  if (use_filter) {
+    uint32_t any_ovf = 0;
+    for (int q = 0; q < P; ++q) any_ovf |= ld_cluster_u32(remote(&sh.part_ovf[0], q));
+    const bool enough = sh.gtotal >= static_cast<uint32_t>(k);
+    fast = enough && any_ovf == 0;
+    if (!enough) {  // the sampled bin was too high: count the remaining keys too
+      for (int i = tid; i < m; i += kThreads) {
+        const int b = lin_bin(key_value(key_at(i)), lo, inv_w);
+        if (b < b_tau) atomicAdd(&sh.hist[b], 1u);
+      }
+      reduce_hist();
+      find_bin(sh, static_cast<uint32_t>(k));
+    }
+  }
+  const int n_lst = min(cnt_w, kListCap);  // this warp's candidates (all of them when fast)
   const int bsel = static_cast<int>(sh.bsel);
   const uint32_t c = sh.ghist[bsel];
   const bool direct = c <= static_cast<uint32_t>(kCandCap);  // the same in every CTA
@@ -326,26 +378,35 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   // the part's count above that bin and its key range within it
   {
     uint32_t kmin = 0xFFFFFFFFu, kmax = 0u, above = 0u;
-    for (int i0 = 0; i0 < m; i0 += 4 * kThreads) {
-      uint32_t kk[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * kThreads + tid;
-        kk[u] = i < m ? key_at(i) : 0u;
+    auto visit = [&](int i, uint32_t key) {
+      const int b = lin_bin(key_value(key), lo, inv_w);
+      above += b > bsel;
+      if (b != bsel) return;
+      kmin = min(kmin, key);
+      kmax = max(kmax, key);
+      if (direct) {
+        const uint32_t slot = atomicAdd(&sh.loc_n, 1u);
+        sh.loc_key[slot] = key;
+        sh.loc_pos[slot] = s0 + i;
       }
+    };
+    if (fast) {  // keys outside the lists lie in bins below b_tau <= bsel
+      for (int j = lane; j < n_lst; j += 32) {
+        const int i = lst[j];
+        visit(i, key_at(i));
+      }
+    } else {
+      for (int i0 = 0; i0 < m; i0 += 4 * kThreads) {
+        uint32_t kk[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * kThreads + tid;
-        if (i >= m) continue;
-        const int b = lin_bin(key_value(kk[u]), lo, inv_w);
-        above += b > bsel;
-        if (b != bsel) continue;
-        kmin = min(kmin, kk[u]);
-        kmax = max(kmax, kk[u]);
-        if (direct) {
-          const uint32_t slot = atomicAdd(&sh.loc_n, 1u);
-          sh.loc_key[slot] = kk[u];
-          sh.loc_pos[slot] = s0 + i;
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * kThreads + tid;
+          kk[u] = i < m ? key_at(i) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * kThreads + tid;
+          if (i < m) visit(i, kk[u]);
         }
       }
     }
@@ -439,14 +500,16 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
 
   // ---- 5. ordered compaction: warp w takes a contiguous run of the part,
   // 32 consecutive keys at a time; ballots give the order within a step
-  const int wrun = (((m + kWarps - 1) / kWarps) + 31) & ~31;
-  const int w0 = min(m, warp * wrun), w1 = min(m, w0 + wrun);
+  // (with candidate lists: warp w takes its list, which holds every selected
+  // key of its run in position order)
+  const int c0 = fast ? 0 : w0, c1 = fast ? n_lst : w1;
+  auto pos_at = [&](int c) -> int { return fast ? static_cast<int>(lst[c]) : c; };
   uint32_t cg = 0, ce = 0;
-  for (int base = w0; base < w1; base += 32) {
-    const int i = base + lane;
-    const uint32_t key = i < w1 ? key_at(i) : 0u;
-    cg += __popc(__ballot_sync(0xFFFFFFFFu, i < w1 && key > thr));
-    ce += __popc(__ballot_sync(0xFFFFFFFFu, i < w1 && key == thr));
+  for (int base = c0; base < c1; base += 32) {
+    const int c = base + lane;
+    const uint32_t key = c < c1 ? key_at(pos_at(c)) : 0u;
+    cg += __popc(__ballot_sync(0xFFFFFFFFu, c < c1 && key > thr));
+    ce += __popc(__ballot_sync(0xFFFFFFFFu, c < c1 && key == thr));
   }
   uint64_t tot;
   const uint64_t wpre = block_exclusive_scan(lane == 0 ? (static_cast<uint64_t>(cg) | (static_cast<uint64_t>(ce) << 32)) : 0ull,
@@ -465,11 +528,11 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   }
   uint32_t g = g_base + static_cast<uint32_t>(wbefore), e = e_base + static_cast<uint32_t>(wbefore >> 32);
   const uint32_t nq = static_cast<uint32_t>(need);
-  const uint32_t lt = (1u << lane) - 1u;
-  for (int base = w0; base < w1; base += 32) {
-    const int i = base + lane;
-    const uint32_t key = i < w1 ? key_at(i) : 0u;
-    const bool gt = i < w1 && key > thr, eq = i < w1 && key == thr;
+  for (int base = c0; base < c1; base += 32) {
+    const int c = base + lane;
+    const int i = c < c1 ? pos_at(c) : 0;
+    const uint32_t key = c < c1 ? key_at(i) : 0u;
+    const bool gt = c < c1 && key > thr, eq = c < c1 && key == thr;
     const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), be = __ballot_sync(0xFFFFFFFFu, eq);
     const uint32_t gi = g + __popc(bg & lt), ei = e + __popc(be & lt);
     if (gt) out[gi + min(ei, nq)] = s0 + i;
@@ -710,8 +773,11 @@ extern "C" dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t*
   }
   const int64_t seg = (ld + p.parts - 1) / p.parts;
   const bool cached = seg <= kSegCap;
-  const int smem = cached ? static_cast<int>(seg * 4) : 0;
-  st = cached ? allow_smem(topk_kernel<true>, kSegCap * 4, g_smem) : allow_smem(topk_kernel<false>, 0, g_smem_u);
+  // the part's keys, then one candidate list per warp (16-bit positions)
+  constexpr int kListBytes = kWarps * kListCap * 2;
+  const int smem = cached ? static_cast<int>(((seg + 7) & ~7) * 4) + kListBytes : 0;
+  st = cached ? allow_smem(topk_kernel<true>, kSegCap * 4 + kListBytes, g_smem)
+              : allow_smem(topk_kernel<false>, 0, g_smem_u);
   if (st != DSA_OK) return st;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(T) * p.parts));

@@ -319,3 +319,36 @@ def test_batch_invariance_with_fixed_splits():
         assert torch.equal(one.topk_idx, full.topk_idx[t0:t1])
         assert torch.equal(one.out, full.out[t0:t1])
         assert torch.equal(one.lse, full.lse[t0:t1])
+
+
+@pytest.mark.parametrize("case", ["sample_misses_the_tail", "ascending_row", "descending_row", "mixed_rows"])
+def test_topk_candidate_lists_and_their_fallbacks(case):
+    """Rows shared by a cluster that keep under 1/8 of their keys record
+    candidates above a bin taken from 1024 samples. These rows defeat that
+    estimate: the sampled positions hold the largest values, so the sampled
+    bin admits fewer than k keys (the histogram is completed and every key
+    visited); sorted rows put all candidates in a few warps' runs (their
+    lists overflow); and a batch mixing such rows with smooth ones."""
+    # 80 rows: two CTAs per row (32768 keys each, 1024-key runs per warp)
+    T, ld, K = 80, 65536, 2048
+    rng = np.random.default_rng(17)
+    vals = rng.random((T, ld), dtype=np.float32)
+    sampled = (np.arange(1024, dtype=np.int64) * ld) // 1024
+    if case == "sample_misses_the_tail":
+        vals[:, sampled] = 9.0 + rng.random((T, 1024), dtype=np.float32)
+    elif case == "ascending_row":
+        vals = np.tile(np.arange(ld, dtype=np.float32), (T, 1)) * 1e-3
+    elif case == "descending_row":
+        vals = np.tile(np.arange(ld, 0, -1, dtype=np.float32), (T, 1)) * 1e-3
+    else:
+        vals[0, sampled] = 9.0
+        vals[2] = np.arange(ld, dtype=np.float32)
+    seq = np.full(T, ld, np.int32)
+    qsl = np.arange(T + 1, dtype=np.int32)
+    got = api.dsa_topk(torch.from_numpy(vals).cuda(), torch.from_numpy(seq).cuda(), torch.from_numpy(qsl).cuda(),
+                       K).cpu().numpy()
+    ref = O.topk(vals, seq, qsl, K)
+    check_topk_sets(got, ref, range(T))
+    for t in range(T):
+        g = got[t][got[t] >= 0]
+        assert len(g) == K and np.all(np.diff(g) > 0)
