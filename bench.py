@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clock-load", action="store_true", help="skip the one-second load before the timed steps")
+    ap.add_argument("--oracle-seconds", type=int, default=0, metavar="N",
+                    help="print the oracle's seconds for N evenly spaced query tokens of the workload and exit (no GPU)")
     return ap.parse_args()
 
 
@@ -152,6 +154,52 @@ def cpu_oracle_step(wl, rows, kv_float=None, q_float=None):
     return time.perf_counter() - t0
 
 
+def cpu_model() -> str:
+    """The host CPU's name as /proc/cpuinfo gives it (x86 or Arm)."""
+    import platform
+
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                fields.setdefault(k.strip(), v.strip())
+        if fields.get("model name"):
+            return fields["model name"]
+        if fields.get("CPU part"):
+            return f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def oracle_rows(T: int, n: int):
+    """n evenly spaced query tokens of T."""
+    n = max(1, min(T, n))
+    return sorted({(i * T) // n for i in range(n)})
+
+
+def oracle_timed(wl, budget_s: float = 10.0):
+    """The oracle on a bounded sample of the workload's query tokens (about
+    budget_s of work): (rows, wall seconds, average busy threads = CPU time / wall)."""
+    per_tok = cpu_oracle_step(wl, [0])
+    rows = oracle_rows(wl.T, int(budget_s / max(per_tok, 1e-6)))
+    c0 = time.process_time()
+    sec = cpu_oracle_step(wl, rows)
+    return rows, sec, (time.process_time() - c0) / max(sec, 1e-9)
+
+
+def oracle_one_thread_seconds(workload: str, n: int):
+    """The same sample in a child process whose BLAS and OpenMP pools hold one thread."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--workload", workload, "--oracle-seconds",
+                            str(n)], env=env, capture_output=True, text=True, timeout=600)
+        return float(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError):
+        return None
+
+
 def blas_threads():
     for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         if os.environ.get(var):
@@ -193,6 +241,10 @@ def main():
     rank, world, local = dist_info()
     from deepseek_sparse_attention_fp8_gb300.inputs import make_workload
 
+    if args.oracle_seconds:
+        wl = make_workload(args.workload)
+        print(cpu_oracle_step(wl, oracle_rows(wl.T, args.oracle_seconds)), flush=True)
+        return
     if args.impl == "reference":
         if rank != 0:
             return
@@ -374,10 +426,13 @@ def main():
     if e2e is not None:
         line["e2e"] = e2e
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sec = cpu_oracle_step(wl, list(range(wl.T)))
-        line["cpu_baseline"] = {"value": wl.T / sec, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-                                "sample": f"one full step ({wl.T} query tokens), numpy float64 oracle, "
-                                          f"{sec:.1f} s"}
+        rows, sec, busy = oracle_timed(wl)
+        sec1 = oracle_one_thread_seconds(wl.name, len(rows))
+        line["cpu_baseline"] = {"value": len(rows) / sec, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"{len(rows)} of {wl.T} query tokens, evenly spaced (full indexer row, "
+                                          f"top-k, attention), numpy float64 oracle, {sec:.1f} s",
+                                "busy_threads": round(busy, 2), "cpu_model": cpu_model(),
+                                "one_thread_value": (len(rows) / sec1) if sec1 else None}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
