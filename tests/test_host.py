@@ -113,3 +113,25 @@ def test_k_quant_and_cache_rejects_bad_arguments(api):
     assert b"null" in lib.dsa_last_error()
     assert call(T=-1) == api.DSA_ERR_INVALID_ARG
     assert call(T=0) == api.DSA_OK  # nothing to do: no device touched
+
+
+def test_header_is_plain_c_and_links(api, tmp_path):
+    """include/dsa.h compiles as pedantic C99 and a C program linked against
+    libdsa.so gets the documented host-side answers (no GPU touched)."""
+    import os
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    libdir = os.path.dirname(api.lib._name)
+    exe = str(tmp_path / "c_abi_check")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(root, "include"),
+                        os.path.join(here, "c_abi_check.c"), "-L", libdir, "-ldsa", f"-Wl,-rpath,{libdir}", "-o", exe],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and "c abi ok" in r.stdout, (r.returncode, r.stdout, r.stderr)
