@@ -78,7 +78,8 @@ def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         try:
-            d = json.load(open(p))
+            with open(p) as f:
+                d = json.load(f)
             hbm = d.get("hbm_gbs") or d.get("hbm_GBs")
             return float(hbm), "measured", d
         except Exception:
@@ -446,7 +447,8 @@ def load_traffic(kernel, workload):
     if not os.path.exists(p):
         return None
     try:
-        d = json.load(open(p))
+        with open(p) as f:
+            d = json.load(f)
         return d.get(workload, {}).get(kernel)
     except Exception:
         return None

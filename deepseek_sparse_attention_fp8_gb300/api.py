@@ -256,5 +256,6 @@ def header_functions():
     """Names of the functions include/dsa.h declares (for export checks)."""
     import re
 
-    text = open(_H).read()
+    with open(_H) as f:
+        text = f.read()
     return sorted(set(re.findall(r"^\s*(?:const char\*|dsa_status_t|size_t|int32_t)\s+(\w+)\s*\(", text, re.M)))

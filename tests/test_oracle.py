@@ -12,7 +12,8 @@ from scipy.special import logsumexp, softmax
 
 from oracle import dsa_oracle as O
 
-GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "hand_examples.json")))
+with open(os.path.join(os.path.dirname(__file__), "golden", "hand_examples.json")) as _f:
+    GOLDEN = json.load(_f)
 
 
 def _f(v):

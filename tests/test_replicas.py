@@ -33,7 +33,7 @@ def _worker(rank, world, port, out):
 def test_two_replicas_take_the_slowest_rank_and_add_tokens():
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork of this (multi-threaded) process
     out = mgr.dict()
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     for rank in range(world):
@@ -41,6 +41,7 @@ def test_two_replicas_take_the_slowest_rank_and_add_tokens():
         assert ms == 0.40
         assert tokens == 64
         assert abs(value - 64 / 0.40e-3) < 1e-6 * value
+    mgr.shutdown()
 
 
 def test_single_process_is_unchanged():
