@@ -4,6 +4,12 @@
 logits and workspace buffers, so that `run()` only enqueues the library's
 kernels (no allocation, no host synchronisation). It is the call a user
 makes per attention layer and batch; the tests and the benchmark drive it.
+
+The per-step inputs (q_idx, w, q, block_table, seq_lens, query_start_loc)
+are views into one device buffer, `inputs`, and the outputs (out, lse) into
+another, `outputs`, each tensor at a 256-byte aligned offset: a caller that
+stages a step's inputs in host memory moves them with one copy each way. The
+caches stay resident in their own buffers.
 """
 from __future__ import annotations
 
@@ -11,6 +17,29 @@ import numpy as np
 import torch
 
 from . import api
+
+
+_ALIGN = 256
+
+
+def _packed(specs, device):
+    """One uint8 device buffer holding tensors of the given (shape, dtype), each
+    at a 256-byte aligned offset; returns (buffer, [views])."""
+    offs, total = [], 0
+    for shape, dtype in specs:
+        nbytes = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+        offs.append((total, nbytes))
+        total += (nbytes + _ALIGN - 1) // _ALIGN * _ALIGN
+    buf = torch.empty(max(total, _ALIGN), dtype=torch.uint8, device=device)
+    views = [buf[o:o + n].view(dtype).view(shape) for (o, n), (shape, dtype) in zip(offs, specs)]
+    return buf, views
+
+
+def _host(a, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype == torch.bfloat16:
+        t = t.view(torch.int16).view(torch.bfloat16)
+    return t if t.dtype == dtype else t.to(dtype)
 
 
 def _dev(a, dtype, device):
@@ -25,18 +54,18 @@ class DsaStep:
         self.wl = wl
         self.device = torch.device(device)
         d = self.device
-        self.q_idx = _dev(wl.q_idx, torch.bfloat16, d)
-        self.w = _dev(wl.w, torch.float32, d)
+        ins = [(wl.q_idx, torch.bfloat16), (wl.w, torch.float32), (wl.q, torch.bfloat16),
+               (wl.block_table, torch.int32), (wl.seq_lens, torch.int32), (wl.query_start_loc, torch.int32)]
+        self.inputs, views = _packed([(np.shape(a), dt) for a, dt in ins], d)
+        for v, (a, dt) in zip(views, ins):
+            v.copy_(_host(a, dt))
+        self.q_idx, self.w, self.q, self.block_table, self.seq_lens, self.qsl = views
         self.k_cache = _dev(wl.k_cache, torch.uint8, d)
-        self.q = _dev(wl.q, torch.bfloat16, d)
         self.kv_cache = _dev(wl.kv_cache, torch.bfloat16, d)
-        self.block_table = _dev(wl.block_table, torch.int32, d)
-        self.seq_lens = _dev(wl.seq_lens, torch.int32, d)
-        self.qsl = _dev(wl.query_start_loc, torch.int32, d)
         self.logits = torch.empty((wl.T, wl.ld), dtype=torch.float32, device=d)
         self.topk_idx = torch.empty((wl.T, wl.index_topk), dtype=torch.int32, device=d)
-        self.out = torch.empty((wl.T, wl.H, wl.Dv), dtype=torch.bfloat16, device=d)
-        self.lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device=d)
+        self.outputs, (self.out, self.lse) = _packed([((wl.T, wl.H, wl.Dv), torch.bfloat16),
+                                                      ((wl.T, wl.H), torch.float32)], d)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=d)
         self.prefill = (wl.max_q_len > 2) if prefill is None else prefill
         self.splits = 1 if self.prefill else (num_kv_splits or api.sparse_mla_auto_splits(wl.T, wl.H, wl.Dv,
