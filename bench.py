@@ -8,8 +8,11 @@ tokens each, 64x128 fp8 indexer, top-2048, 128-head 576/512 MLA). Prints one
 JSON line. `value` is decode tokens/s over the device-timed step with inputs
 resident in HBM and L2 flushed between steps; `e2e` repeats it through the
 public API with per-step inputs copied from pinned host memory and the output
-read back. Under torchrun every rank runs an independent replica (the step
-has no exchange), ranks are timed with a barrier and the max is taken.
+read back. `kernels` times each phase alone, `roofline` relates the dominant
+one to the HBM peak, `producer` times the key-cache writer (outside the step)
+and `cpu_baseline` the oracle on a bounded sample of the workload's tokens.
+Under torchrun every rank runs an independent replica (the step has no
+exchange), ranks are timed with a barrier and the max is taken.
 """
 from __future__ import annotations
 
