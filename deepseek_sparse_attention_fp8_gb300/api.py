@@ -24,6 +24,7 @@ lib = ctypes.CDLL(LIB)
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE, DSA_ERR_CUDA = range(5)
 DSA_DEVERR_BLOCK_OOB, DSA_DEVERR_INDEX_OOB, DSA_DEVERR_TIMEOUT, DSA_DEVERR_SEQ_LEN = 1, 2, 4, 8
+DSA_KV_SPLITS_BATCH_INVARIANT = -1
 
 _p = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -43,6 +44,7 @@ _SIGS = {
     "dsa_topk": ([_p, _i64, _p, _p, _i32, _i32, _i32, _p, _p, _sz, _p], _i32),
     "sparse_mla_workspace_size": ([_i32, _i32, _i32, _i32], _sz),
     "sparse_mla_auto_splits": ([_i32, _i32, _i32, _i32], _i32),
+    "sparse_mla_num_splits": ([_i32, _i32, _i32, _i32, _i32], _i32),
     "sparse_mla_decode": ([_p, _p, _i64, _i32, _p, _i32, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32,
                            _i32, _p, _p, _p, _sz, _p, _p], _i32),
     "sparse_mla_fixed_scratch_bytes": ([], _sz),
@@ -181,6 +183,12 @@ def sparse_mla_auto_splits(T: int, H: int, Dv: int, index_topk: int) -> int:
     return int(lib.sparse_mla_auto_splits(T, H, Dv, index_topk))
 
 
+def sparse_mla_num_splits(T: int, H: int, Dv: int, index_topk: int, num_kv_splits: int) -> int:
+    """The split count sparse_mla_decode uses for num_kv_splits (0 = automatic,
+    DSA_KV_SPLITS_BATCH_INVARIANT = fixed by index_topk alone, n = n)."""
+    return int(lib.sparse_mla_num_splits(T, H, Dv, index_topk, num_kv_splits))
+
+
 def _mla_common(q, kv_cache, block_table, seq_lens, query_start_loc, topk_idx, out, lse, dev_status):
     _need(q, torch.bfloat16, "q", 3)
     _need(kv_cache, torch.bfloat16, "kv_cache", 3)
@@ -200,18 +208,20 @@ def _mla_common(q, kv_cache, block_table, seq_lens, query_start_loc, topk_idx, o
 
 def sparse_mla_decode(q, kv_cache, block_table, seq_lens, query_start_loc, topk_idx, softmax_scale, dv, out,
                       lse=None, num_kv_splits=0, workspace=None, dev_status=None, stream=None):
-    """a3 + a4: out [T,H,Dv] (bf16) of sparse MLA over kv_cache [blocks, block_size, Dk]."""
+    """a3 + a4: out [T,H,Dv] (bf16) of sparse MLA over kv_cache [blocks, block_size, Dk].
+    num_kv_splits: 0 automatic (depends on the batch size), -1
+    (DSA_KV_SPLITS_BATCH_INVARIANT) fixed by index_topk alone, or a count."""
     num_blocks, block_size, Dk, T, H = _mla_common(q, kv_cache, block_table, seq_lens, query_start_loc, topk_idx,
                                                    out, lse, dev_status)
     K = topk_idx.shape[1]
-    splits = num_kv_splits if num_kv_splits else sparse_mla_auto_splits(T, H, dv, K)
+    splits = sparse_mla_num_splits(T, H, dv, K, num_kv_splits)
     need = sparse_mla_workspace_size(T, H, dv, splits)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib.sparse_mla_decode(_ptr(q), _ptr(kv_cache), block_size * Dk, num_blocks, _ptr(block_table),
                                block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc), _ptr(topk_idx),
-                               seq_lens.shape[0], T, H, Dk, dv, K, block_size, softmax_scale, splits, _ptr(out),
+                               seq_lens.shape[0], T, H, Dk, dv, K, block_size, softmax_scale, num_kv_splits, _ptr(out),
                                _ptr(lse), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
     _check(st, "sparse_mla_decode")
     return out

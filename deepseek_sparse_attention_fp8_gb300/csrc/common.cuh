@@ -4,8 +4,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 
 #include "../../include/dsa.h"
 
@@ -29,17 +31,33 @@ dsa_status_t make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, co
 // Converts a pending launch error into DSA_ERR_CUDA.
 dsa_status_t check_launch(const char* what);
 
-// Raises the dynamic shared-memory limit of a kernel once per process.
+// Per-device record of which kernels have had their shared-memory
+// attributes set. The flags are atomics and the first setting on a device is
+// made under the mutex, so concurrent first calls and several devices in one
+// process are both safe.
+constexpr int kMaxDeviceOrdinals = 64;
+struct FuncAttrOnce {
+  std::mutex mu;
+  std::atomic<bool> done[kMaxDeviceOrdinals] = {};
+};
+
+// Raises the dynamic shared-memory limit of a kernel once per device.
 template <typename K>
-dsa_status_t allow_smem(K kernel, int bytes, bool& done) {
-  if (done) return DSA_OK;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+dsa_status_t allow_smem(K kernel, int bytes, FuncAttrOnce& once) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDeviceOrdinals) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  if (once.done[dev].load(std::memory_order_acquire)) return DSA_OK;
+  std::lock_guard<std::mutex> lock(once.mu);
+  if (once.done[dev].load(std::memory_order_relaxed)) return DSA_OK;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "cudaFuncSetAttribute(%d bytes): %s", bytes, cudaGetErrorString(e));
   // every kernel of the library asks for the same (largest) shared-memory
   // carveout, so consecutive launches never wait for the SMs to be re-split
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "cudaFuncSetAttribute(carveout): %s", cudaGetErrorString(e));
-  done = true;
+  once.done[dev].store(true, std::memory_order_release);
   return DSA_OK;
 }
 

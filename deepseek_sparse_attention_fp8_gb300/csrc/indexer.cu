@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   if (n_comp > 0 && warp == kMmaWarp) tmem_dealloc(tmem, tmem_cols);
 }
 
-bool g_smem_set[3] = {false, false, false};
+FuncAttrOnce g_smem_set[3];
 
 }  // namespace
 }  // namespace dsa

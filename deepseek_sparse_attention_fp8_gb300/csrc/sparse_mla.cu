@@ -16,15 +16,16 @@
 // Per 64-key tile, in each CTA:
 //   S_r = Q_r K_r^T   tcgen05 kind::f16, M=128, N=64, A (this CTA's q dims)
 //                     in tensor memory, B from the swizzled KV stage;
-//   exchange          S_r rounded to fp16 goes to the peer over DSMEM
-//                     (st.async); both CTAs form S = f16(S_0) + f16(S_1);
+//   exchange          S_r, scaled by softmax_scale * log2(e), goes to the peer
+//                     in fp32 over DSMEM (st.async); both CTAs form
+//                     S = S_0 + S_1 (log2 units) and agree bit for bit;
 //   softmax           thread = head row; two warp groups take alternate
 //                     tiles; lazy rescaling of O (only when the row maximum
 //                     grows by more than 2^8);
-//   O_r += P V_r      M=128, N=256, fp32 accumulator in tensor memory.
+//   O_r += P V_r      M=128, N=256, A = P (bf16) in tensor memory, fp32
+//                     accumulator in tensor memory.
 // Warp roles: 8 softmax/epilogue warps, 4 producer warps (TMA), 1 MMA warp.
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <cmath>
@@ -52,7 +53,8 @@ constexpr long long kWaitLimitCycles = 2000000000ll;
 constexpr int kQStage = 2;  // q is staged in KV stages 2 and 3
 static_assert(kMaxSlots <= 256 * 8, "the softmax warps resolve all slots in one pass");
 static_assert(kQStage + 2 <= kStages, "q staging needs two KV stages");
-constexpr int kXPitch = 64 * 2 + 16;      // bytes per row of an exchange buffer (fp16 scores)
+constexpr int kXRow = 64 * 4;             // bytes of one row's 64 fp32 scores in an exchange buffer
+constexpr int kXChunk = 128 * 16;         // stride of a 16-byte chunk column (128 rows) in an exchange buffer
 
 // kPair: the two CTAs of a cluster split the Dk dims and the value dims:
 // rank r owns value dims [r*kDvc, (r+1)*kDvc) = K-blocks [4r, 4r+4) (64 dims
@@ -84,9 +86,8 @@ struct MlaSmem {
   static constexpr int kKvStage = kKvHalf + (C::kRopeHalf ? kTileKeys * 64 : 0);
   static constexpr int kQHalf = C::kRopeHalf ? 128 * 64 : 0;  // q's rope half: 128 heads x 64 B
   static constexpr int kKv = 0;
-  static constexpr int kP = kKv + kStages * kKvStage;
-  static constexpr int kX = kP + 16384;
-  static constexpr int kXBuf = 128 * kXPitch;
+  static constexpr int kX = kKv + kStages * kKvStage;
+  static constexpr int kXBuf = 128 * kXRow;
   static constexpr int kRow = kX + (C::kPair ? kXBufs * kXBuf : 0);
   static constexpr int kLive = kRow + kMaxSlots * 4;
   static constexpr int kCoord = kLive + kStages * kTileKeys;
@@ -116,15 +117,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-__device__ __forceinline__ float2 unpack_f16(uint32_t v) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&v));
-}
-
 __device__ __forceinline__ int find_request(const int32_t* qsl, int B, int t) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {
@@ -143,7 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   using C = MlaCfg<DK, DV>;
   using L = MlaSmem<DK, DV>;
   constexpr int kSplitDv = C::kPair ? 2 : 1;
+  // tensor-memory columns: S (fp32), O (fp32), Q (bf16 pairs), P (bf16 pairs)
   constexpr uint32_t kColS = 0, kColO = kTileKeys, kColQ = kTileKeys + C::kDvc;
+  constexpr uint32_t kColP = kColQ + C::kNkb * 32 + (C::kRopeHalf ? 16 : 0);
+  static_assert(kColP + kTileKeys / 2 <= C::kTmemCols, "tensor-memory columns overflow");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -165,7 +160,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   const int rope_x = C::kRopeX + 32 * r;           // its rope half (dims), when there is one
 
   uint8_t* kv_sm = smem + L::kKv;
-  uint8_t* p_sm = smem + L::kP;
   uint8_t* x_sm = smem + L::kX;
   int* row_sm = reinterpret_cast<int*>(smem + L::kRow);
   uint16_t* live_m = reinterpret_cast<uint16_t*>(smem + L::kLive);  // [stage][producer warp]: live-key bits
@@ -402,7 +396,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     tc_fence_after();
     const uint32_t idesc_qk = idesc_bf16(128, kTileKeys, false, false);
     const uint32_t idesc_pv = idesc_bf16(128, C::kDvc, false, true);
-    const uint32_t p0s = smem_u32(p_sm);
     auto issue_qk = [&](int i) {  // this CTA's part of S = Q K^T
       const int st = i % kStages;
       // descriptors differ only in the start-address field (16-byte units)
@@ -427,11 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       const int st = i % kStages;
       // value dims = this CTA's first K-blocks
       const uint64_t vd = smem_desc(smem_u32(kv_sm + st * L::kKvStage), L::kKvKb, 1024, kSwizzle128B);
-      const uint64_t pd = smem_desc(p0s, 16, 1024, kSwizzle128B);
+      // A = P from tensor memory: 16 keys (8 columns of bf16 pairs) per MMA
 #pragma unroll
       for (int ks = 0; ks < kTileKeys / 16; ++ks)
-        mma_bf16_ss(tmem + kColO, pd + static_cast<uint64_t>((ks * 32) >> 4), vd + static_cast<uint64_t>((ks * 2048) >> 4),
-                    idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+        mma_bf16_ts(tmem + kColO, tmem + kColP + ks * 8, vd + static_cast<uint64_t>((ks * 2048) >> 4), idesc_pv,
+                    (i > 0 || ks > 0) ? 1u : 0u);
       mma_commit(&kv_empty[st]);
       mma_commit(&o_done[i & 1]);
       if (i == n_tiles - 1) mma_commit(&o_final);
@@ -484,7 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     const bool leader = (tid & 127) == 0;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     float* m_hand = reinterpret_cast<float*>(smem + L::kRed);  // [group][row]: m after the group's latest tile
-    const uint8_t* x_mine = x_sm + g * L::kXBuf + h * kXPitch;
+    // this group's exchange buffer is chunk-major: 16-byte chunk c (scores
+    // 4c..4c+3) of row h sits at c * 2048 + h * 16, so a warp's accesses to
+    // one chunk are 512 contiguous bytes
+    const uint8_t* x_mine = x_sm + g * L::kXBuf + h * 16;
     uint32_t x_peer = 0, peer_x_full = 0, peer_x_empty = 0;
     if constexpr (C::kPair) {
       x_peer = mapa_shared(smem_u32(x_mine), static_cast<uint32_t>(r ^ 1));
@@ -502,16 +498,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       }
       tc_fence_after();
       if constexpr (C::kPair) {
-        // this CTA's partial scores, rounded to fp16, go to the peer; both
-        // CTAs then add the same two fp16 partials and agree bit for bit
-        uint32_t hv[32];
+        // this CTA's half-scores, scaled to log2 units, go to the peer in
+        // fp32; both CTAs then add the same two fp32 halves (addition is
+        // commutative) and agree bit for bit
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t sv[32];
           tmem_ld32_sync(lane_base + kColS + half * 32, sv);
 #pragma unroll
-          for (int x = 0; x < 16; ++x)
-            hv[half * 16 + x] = pack_f16_sat(__uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]));
+          for (int x = 0; x < 32; ++x) s[half * 32 + x] = __uint_as_float(sv[x]) * p.scale_log2;
         }
         tc_fence_before();
         __syncwarp();
@@ -522,28 +517,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
           if (lane == 0) abort_now();
           break;
         }
-        if (leader) mbar_arrive_expect_tx(&x_full[g], 128 * kTileKeys * 2);  // the peer's whole partial tile
+        if (leader) mbar_arrive_expect_tx(&x_full[g], 128 * kXRow);  // the peer's whole tile of half-scores
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_async_v4(x_peer + c * 16, peer_x_full, hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
+        for (int c = 0; c < 16; ++c)
+          st_async_v4(x_peer + c * kXChunk, peer_x_full, __float_as_uint(s[4 * c]), __float_as_uint(s[4 * c + 1]),
+                      __float_as_uint(s[4 * c + 2]), __float_as_uint(s[4 * c + 3]));
         if (!mbar_wait_cluster(&x_full[g], u & 1)) {
           if (lane == 0) abort_now();
           break;
         }
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 w4 = *reinterpret_cast<const uint4*>(x_mine + c * 16);
-          const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-          for (int y = 0; y < 4; ++y) {
-            const float2 f = unpack_f16(w[y]);
-            const float2 o = unpack_f16(hv[4 * c + y]);
-            s[8 * c + 2 * y] = o.x + f.x;
-            s[8 * c + 2 * y + 1] = o.y + f.y;
-          }
+        for (int c = 0; c < 16; ++c) {
+          const float4 f = *reinterpret_cast<const float4*>(x_mine + c * kXChunk);
+          s[4 * c] += f.x;
+          s[4 * c + 1] += f.y;
+          s[4 * c + 2] += f.z;
+          s[4 * c + 3] += f.w;
         }
-        // the loaded values are consumed above, so the loads have completed
-        // when the (fence-free) arrival tells the peer it may overwrite them
+        // the loaded values are consumed above (the empty asm takes the sum of
+        // the last chunk, so it cannot issue before that load has returned),
+        // so the loads have completed when the (fence-free) arrival tells the
+        // peer it may overwrite them
+        asm volatile("" ::"f"(s[kTileKeys - 1]) : "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive_remote_relaxed(peer_x_empty);
       } else {
@@ -552,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
           uint32_t sv[32];
           tmem_ld32_sync(lane_base + kColS + half * 32, sv);
 #pragma unroll
-          for (int x = 0; x < 32; ++x) s[half * 32 + x] = __uint_as_float(sv[x]);
+          for (int x = 0; x < 32; ++x) s[half * 32 + x] = __uint_as_float(sv[x]) * p.scale_log2;
         }
         tc_fence_before();
         __syncwarp();
@@ -563,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
         break;
       }
       const uint64_t live = *reinterpret_cast<const uint64_t*>(live_m + st * 4);
-      float mt = -INFINITY;  // the tile's raw row maximum (scale > 0)
+      float mt = -INFINITY;  // the tile's row maximum (log2 units)
 #pragma unroll
       for (int x = 0; x < kTileKeys; ++x) {
         if (!((live >> x) & 1u)) s[x] = -INFINITY;
@@ -577,9 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
         }
         m_prev = m_hand[(g ^ 1) * 128 + h];
       }
-      const float mt2 = mt * p.scale_log2;
-      const bool rescale = mt2 > m_prev + kRescaleThreshold;
-      const float m_new = rescale ? mt2 : m_prev;
+      const bool rescale = mt > m_prev + kRescaleThreshold;
+      const float m_new = rescale ? mt : m_prev;
       m_hand[g * 128 + h] = m_new;
       __syncwarp();
       if (lane == 0) mbar_arrive(&m_bar[g]);
@@ -589,8 +583,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
       for (int x = 0; x < 32; ++x) {
-        const float a = ex2_approx(fmaf(s[2 * x], p.scale_log2, neg_m));
-        const float c = ex2_approx(fmaf(s[2 * x + 1], p.scale_log2, neg_m));
+        const float a = ex2_approx(s[2 * x] + neg_m);
+        const float c = ex2_approx(s[2 * x + 1] + neg_m);
         const __nv_bfloat162 pb = __floats2bfloat162_rn(a, c);
         // the normaliser sums the bf16 weights that the PV product uses
         ps0 += __bfloat162float(pb.x);
@@ -610,10 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
         }
         tc_fence_after();
       }
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(p_sm + sw128_offset(h, c)) =
-            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+      tmem_st32(lane_base + kColP, pw);  // this row's 64 weights as 32 bf16 pairs
       if (i >= 1 && __any_sync(0xFFFFFFFFu, rescale)) {
         const float alpha = rescale ? ex2_approx(m_prev - m_new) : 1.f;
 #pragma unroll 1
@@ -624,9 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
           for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
           tmem_st32(lane_base + kColO + c, o);
         }
-        tmem_st_wait();
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();  // P (and a rescaled O) are in tensor memory before PV is issued
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full);
@@ -772,7 +762,7 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const float* __restrict_
   if (v == 0 && lse != nullptr) lse[row] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
 }
 
-bool g_smem_merge = false;
+FuncAttrOnce g_smem_merge;
 
 dsa_status_t launch_merge(const MlaParams& p, int Dv, float* lse, cudaStream_t s) {
   dsa_status_t st = allow_smem(mla_merge_kernel, 0, g_smem_merge);
@@ -794,7 +784,7 @@ dsa_status_t launch_merge(const MlaParams& p, int Dv, float* lse, cudaStream_t s
   return DSA_OK;
 }
 
-bool g_smem_big = false, g_smem_tiny = false;
+FuncAttrOnce g_smem_big, g_smem_tiny;
 
 int dv_split_for(int Dv) { return Dv == 512 ? 2 : 1; }
 
@@ -949,6 +939,14 @@ extern "C" int32_t sparse_mla_auto_splits(int32_t T, int32_t H, int32_t Dv, int3
   return best;
 }
 
+extern "C" int32_t sparse_mla_num_splits(int32_t T, int32_t H, int32_t Dv, int32_t index_topk,
+                                         int32_t num_kv_splits) {
+  if (num_kv_splits > 0) return num_kv_splits;
+  if (num_kv_splits == DSA_KV_SPLITS_BATCH_INVARIANT)
+    return index_topk > 0 ? (index_topk + kMaxSlots - 1) / kMaxSlots : 1;  // depends on index_topk alone
+  return sparse_mla_auto_splits(T, H, Dv, index_topk);
+}
+
 extern "C" dsa_status_t sparse_mla_decode(const void* q, const void* kv_cache, int64_t kv_block_stride,
                                           int32_t num_blocks, const int32_t* block_table, int32_t bt_stride,
                                           const int32_t* seq_lens, const int32_t* query_start_loc,
@@ -960,9 +958,9 @@ extern "C" dsa_status_t sparse_mla_decode(const void* q, const void* kv_cache, i
                              query_start_loc, topk_idx, B, T, H, Dk, Dv, index_topk, block_size, softmax_scale, out,
                              "sparse_mla_decode");
   if (st != DSA_OK || T == 0) return st;
-  if (num_kv_splits < 0 || num_kv_splits > 32)
-    return fail(DSA_ERR_INVALID_ARG, "sparse_mla_decode: num_kv_splits %d not in [0, 32]", num_kv_splits);
-  int splits = num_kv_splits == 0 ? sparse_mla_auto_splits(T, H, Dv, index_topk) : num_kv_splits;
+  if (num_kv_splits < DSA_KV_SPLITS_BATCH_INVARIANT || num_kv_splits > 32)
+    return fail(DSA_ERR_INVALID_ARG, "sparse_mla_decode: num_kv_splits %d not in [-1, 32]", num_kv_splits);
+  const int splits = sparse_mla_num_splits(T, H, Dv, index_topk, num_kv_splits);
   if ((index_topk + splits - 1) / splits > kMaxSlots)
     return fail(DSA_ERR_UNSUPPORTED, "sparse_mla_decode: %d top-k slots per split exceed %d", (index_topk + splits - 1) / splits,
                 kMaxSlots);
@@ -1048,14 +1046,20 @@ extern "C" dsa_status_t sparse_mla_decode_fixed_scratch(
     int32_t bt_stride, const int32_t* seq_lens, const int32_t* query_start_loc, const int32_t* topk_idx, int32_t B,
     int32_t T, int32_t H, int32_t Dk, int32_t Dv, int32_t index_topk, int32_t block_size, float softmax_scale,
     int32_t num_kv_splits, void* out, float* lse, int32_t* dev_status, dsa_stream_t stream) {
-  if (num_kv_splits < 0 || num_kv_splits > 32)
-    return fail(DSA_ERR_INVALID_ARG, "sparse_mla_decode_fixed_scratch: num_kv_splits %d not in [0, 32]",
+  if (num_kv_splits < DSA_KV_SPLITS_BATCH_INVARIANT || num_kv_splits > 32)
+    return fail(DSA_ERR_INVALID_ARG, "sparse_mla_decode_fixed_scratch: num_kv_splits %d not in [-1, 32]",
                 num_kv_splits);
   if (T <= 0 || H <= 0 || Dv <= 0 || index_topk <= 0)  // nothing to split: no scratch needed
     return sparse_mla_decode(q, kv_cache, kv_block_stride, num_blocks, block_table, bt_stride, seq_lens,
                              query_start_loc, topk_idx, B, T, H, Dk, Dv, index_topk, block_size, softmax_scale,
                              num_kv_splits, out, lse, nullptr, 0, dev_status, stream);
-  const int32_t splits = num_kv_splits == 0 ? sparse_mla_auto_splits(T, H, Dv, index_topk) : num_kv_splits;
+  int32_t splits = sparse_mla_num_splits(T, H, Dv, index_topk, num_kv_splits);
+  if (num_kv_splits == 0) {
+    // automatic count: the largest one, down to the fewest splits the slot
+    // limit allows, whose partials fit the fixed scratch
+    const int32_t fewest = (index_topk + kMaxSlots - 1) / kMaxSlots;
+    while (splits > fewest && sparse_mla_workspace_size(T, H, Dv, splits) > kFixedScratchBytes) --splits;
+  }
   const size_t need = sparse_mla_workspace_size(T, H, Dv, splits);
   if (need > kFixedScratchBytes)
     return fail(DSA_ERR_WORKSPACE,

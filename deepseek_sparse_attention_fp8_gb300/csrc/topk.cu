@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const TopkParams p) 
   }
 }
 
-bool g_smem = false, g_smem_u = false;
+FuncAttrOnce g_smem, g_smem_u;
 
 // CTAs per row: more only for long rows (at least 8192 keys per CTA) while
 // they fill the GPU once (at most 8), and enough that a part fits the

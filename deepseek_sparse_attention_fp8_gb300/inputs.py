@@ -92,9 +92,11 @@ def _e4m3_codes(x: np.ndarray) -> np.ndarray:
 
 
 def make_workload(name: str, seed: int | None = None, *, B: int | None = None, L=None, q_len: int | None = None,
-                  index_topk: int | None = None, ld_pad: int = 128, lens=None, block_size: int = 64) -> Workload:
+                  index_topk: int | None = None, ld_pad: int = 128, lens=None, block_size: int = 64,
+                  q_std: float = 1.0) -> Workload:
     """Build one of the named workloads (optionally overriding a few sizes
-    for smaller parity cases). `lens` gives explicit per-request lengths."""
+    for smaller parity cases). `lens` gives explicit per-request lengths;
+    `q_std` the standard deviation of the MLA queries (1 in every workload)."""
     spec = dict(WORKLOADS[name])
     if B is not None:
         spec["B"] = B
@@ -169,7 +171,7 @@ def make_workload(name: str, seed: int | None = None, *, B: int | None = None, L
 
     q_idx = _bf16_bits(rng.standard_normal((T, Hi, Di), dtype=np.float32))
     w = (rng.standard_normal((T, Hi), dtype=np.float32) / np.float32(math.sqrt(Hi))).astype(np.float32)
-    q = _bf16_bits(rng.standard_normal((T, H, Dk), dtype=np.float32))
+    q = _bf16_bits(rng.standard_normal((T, H, Dk), dtype=np.float32) * np.float32(q_std))
 
     ld = int(max(seq_lens)) if Bn else 1
     ld = (ld + ld_pad - 1) // ld_pad * ld_pad

@@ -68,8 +68,9 @@ class DsaStep:
                                                       ((wl.T, wl.H), torch.float32)], d)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=d)
         self.prefill = (wl.max_q_len > 2) if prefill is None else prefill
-        self.splits = 1 if self.prefill else (num_kv_splits or api.sparse_mla_auto_splits(wl.T, wl.H, wl.Dv,
-                                                                                          wl.index_topk))
+        # num_kv_splits: 0 automatic, -1 batch-invariant (fixed by index_topk), n > 0 that many
+        self.splits = 1 if self.prefill else api.sparse_mla_num_splits(wl.T, wl.H, wl.Dv, wl.index_topk,
+                                                                         num_kv_splits)
         ws_topk = api.dsa_topk_workspace_size(wl.T, wl.ld, wl.index_topk)
         ws_mla = api.sparse_mla_workspace_size(wl.T, wl.H, wl.Dv, self.splits)
         self.ws_topk = torch.empty(max(ws_topk, 16), dtype=torch.uint8, device=d)

@@ -81,6 +81,10 @@ typedef enum {
 #define DSA_DEVERR_TIMEOUT 4u   /* a bounded wait inside a kernel ran out */
 #define DSA_DEVERR_SEQ_LEN 8u   /* seq_lens[b] < q_len_b, or larger than the block table can hold */
 
+/* num_kv_splits value of sparse_mla_decode that makes the split count depend
+ * on index_topk alone, so a token's out and lse do not depend on the batch. */
+#define DSA_KV_SPLITS_BATCH_INVARIANT (-1)
+
 /* One-line reason for the last non-OK status returned on this thread. */
 const char* dsa_last_error(void);
 
@@ -169,17 +173,39 @@ dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t* seq_lens, 
  *             treated as empty and sets DSA_DEVERR_INDEX_OOB.
  *   out       bf16 [T, H, Dv]: softmax(scale * q . kv[sel]) @ kv[sel, :Dv]
  *   lse       fp32 [T, H] natural-log sum-exp of the scaled scores, or NULL.
- * num_kv_splits: 0 = pick automatically, else 1..32. With S > 1 the top-k
- * slots are cut into S contiguous ranges of ceil(index_topk / S); each split
- * writes fp32 partials to `workspace` (sparse_mla_workspace_size bytes) and a
- * merge kernel combines them. Empty slots score the finite sentinel -1e30 and
- * carry weight 0, so an all-empty split contributes nothing and no NaN
- * appears; a token with no selected row gets out = 0 and lse = -inf.
- * Supported: H <= 128, (Dk, Dv) in {(576, 512), (80, 64)}.
+ * num_kv_splits: the number S of KV splits.
+ *   1..32  that many splits;
+ *   0      chosen from T, H, Dv, index_topk and the SM count
+ *          (sparse_mla_auto_splits). The count then depends on the batch
+ *          size, and so do the bf16 roundings of a token's out and lse;
+ *   DSA_KV_SPLITS_BATCH_INVARIANT (-1)
+ *          ceil(index_topk / 2048) splits, fixed by index_topk alone: a
+ *          token's out and lse are bit-identical in any batch (every kernel
+ *          of the step works on one token of one request at a time). With
+ *          index_topk <= 2048 this is the single-pass path (the batch-invariant
+ *          mode of vLLM PR #38476, Limitations: force one KV split).
+ * sparse_mla_num_splits() resolves 0 and -1 to the count a call will use.
+ * With S > 1 the top-k slots are cut into S contiguous ranges of
+ * ceil(index_topk / S); each split writes fp32 partials to `workspace`
+ * (sparse_mla_workspace_size(T, H, Dv, S) bytes) and a merge kernel combines
+ * them. Empty slots score the finite sentinel -1e30 and carry weight 0, so an
+ * all-empty split contributes nothing and no NaN appears; a token with no
+ * selected row gets out = 0 and lse = -inf.
+ * Score arithmetic (Dk = 576): the dims of a row are split between two CTAs
+ * (latent [0,256) with rope [512,544), latent [256,512) with rope [544,576));
+ * each CTA's half-score comes from an fp32 tensor-core accumulator, is scaled
+ * by softmax_scale * log2(e) in fp32 and exchanged in fp32, and the two
+ * halves are added in fp32 (no input-range limit beyond fp32's).
+ * Supported: H <= 128, (Dk, Dv) in {(576, 512), (80, 64)}, 1 <= S and
+ * ceil(index_topk / S) <= 2048.
  * (vLLM PR #38476 Changes 3.)
  */
+/* Workspace bytes of S = num_kv_splits splits (an actual count: 0 when S <= 1). */
 size_t sparse_mla_workspace_size(int32_t T, int32_t H, int32_t Dv, int32_t num_kv_splits);
+/* The automatic split count: a wave-count cost model over the SM count. */
 int32_t sparse_mla_auto_splits(int32_t T, int32_t H, int32_t Dv, int32_t index_topk);
+/* The split count sparse_mla_decode uses for this num_kv_splits argument. */
+int32_t sparse_mla_num_splits(int32_t T, int32_t H, int32_t Dv, int32_t index_topk, int32_t num_kv_splits);
 dsa_status_t sparse_mla_decode(const void* q, const void* kv_cache, int64_t kv_block_stride, int32_t num_blocks,
                                const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
                                const int32_t* query_start_loc, const int32_t* topk_idx, int32_t B, int32_t T,
@@ -200,24 +226,27 @@ dsa_status_t sparse_mla_prefill(const void* q, const void* kv_cache, int64_t kv_
                                 dsa_stream_t stream);
 
 /*
- * Split-KV sparse MLA decode that allocates nothing, for callers that cannot
- * call cudaMalloc when they run the step: code inside a CUDA-graph capture
- * region, allocator-free serving runtimes that own all device memory up front,
- * and host environments that may not create device allocations. The pages
- * have no counterpart of this entry point; it is a deployment convenience.
+ * Split-KV sparse MLA decode that allocates nothing. It serves callers that
+ * may not call cudaMalloc when they run the step: serving runtimes that hand
+ * all device memory to their own allocator at start-up and forbid later
+ * allocations, and host environments (plugins, sandboxed runtimes) that are
+ * not allowed to create device allocations. The pages have no counterpart of
+ * this entry point; it is a deployment convenience.
  *
  * Same arguments and results as sparse_mla_decode, minus the workspace: the
  * split partials go to a fixed scratch array of sparse_mla_fixed_scratch_bytes()
  * bytes (24 MiB) that the library reserves in device memory on every GPU that
- * loads it, held until the process exits. A request whose partials
- * (sparse_mla_workspace_size for the chosen number of splits) exceed it is
- * rejected with DSA_ERR_WORKSPACE and launches nothing.
+ * loads it, held until the process exits. With num_kv_splits = 0 the
+ * automatic count is lowered, down to the fewest splits allowed, until the
+ * partials fit. A request whose partials (sparse_mla_workspace_size for the
+ * resulting number of splits) still exceed the array is rejected with
+ * DSA_ERR_WORKSPACE and launches nothing.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) for that device; make that first call before any
  *     stream capture that includes this entry point.
- *   - All calls share the one array. Calls that may overlap on the GPU (on
- *     different streams, or in parallel graphs) race on it and must be
- *     serialised by the caller.
+ *   - All calls share the one array, which keeps the last call's contents.
+ *     Calls that may overlap on the GPU (on different streams, or in parallel
+ *     graphs) race on it and must be serialised by the caller.
  *   - Nothing in the array needs to start at zero: every partial the merge
  *     reads is written first in the same call.
  */

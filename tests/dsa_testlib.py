@@ -12,9 +12,13 @@ from oracle import dsa_oracle as O
 # floored at 1e-2 of the row's rms.
 LOGIT_RTOL = 2e-2
 LOGIT_FLOOR = 1e-2
-# Attention output (bf16): max abs 2e-2, mean abs 2e-3.
+# Attention output (bf16): max abs 2e-2, mean abs 2e-3. At index_topk = 2048
+# the outputs are small (|out| ~ 1e-2), so the error relative to the output's
+# rms is bounded too: bf16 output rounding alone gives ~2e-3, and the kernel's
+# bf16 softmax weights add about as much again.
 ATT_MAX_ABS = 2e-2
 ATT_MEAN_ABS = 2e-3
+ATT_RMS_REL = 1e-2
 
 
 def oracle_q_quant(wl):
@@ -66,15 +70,21 @@ def oracle_attention(wl, topk_idx, rows=None, splits=1):
 
 
 def check_attention(got, ref, rows, got_lse=None, ref_lse=None):
+    """Max and mean absolute error and rms(g - r) / rms(r) within bounds;
+    returns the three."""
     g = got[rows].astype(np.float64)
     r = ref[rows]
     assert np.all(np.isfinite(g)), "non-finite attention output"
     err = np.abs(g - r)
     assert err.max() <= ATT_MAX_ABS, f"max abs error {err.max():.3g}"
     assert err.mean() <= ATT_MEAN_ABS, f"mean abs error {err.mean():.3g}"
+    rms_r = np.sqrt(np.mean(r ** 2))
+    rms_rel = float(np.sqrt(np.mean(err ** 2)) / rms_r) if rms_r > 0 else 0.0
+    if rms_r > 0:
+        assert rms_rel <= ATT_RMS_REL, f"rms(g - r) / rms(r) = {rms_rel:.3g}"
     if got_lse is not None:
         gl, rl = got_lse[rows].astype(np.float64), ref_lse[rows]
         fin = np.isfinite(rl)
         assert np.array_equal(np.isfinite(gl), fin)
         assert np.all(np.abs(gl[fin] - rl[fin]) <= 1e-3 * np.maximum(1.0, np.abs(rl[fin])))
-    return float(err.max()), float(err.mean())
+    return float(err.max()), float(err.mean()), rms_rel

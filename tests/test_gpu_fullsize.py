@@ -55,11 +55,16 @@ def test_decode_b8_l131072_splits_agree():
         outs[s] = step.out.float().cpu().numpy()
     # the split count changes the summation order and the running maximum the
     # bf16 softmax weights are taken against, so results differ by bf16
-    # rounding; a lost or doubled split would move outputs by far more than
-    # these bounds (a twentieth of the oracle's mean tolerance)
+    # rounding. Measured on GB300 for this workload (the kernels are
+    # deterministic): splits 8 and 32 against 1 differ by at most 4.88e-4 (one
+    # bf16 ulp of the largest outputs, 2^-11) and by 2.17e-5 / 2.21e-5 on
+    # average; the bounds are twice those. Near-zero outputs (sums that
+    # cancel) differ by many of their own ulps, so no per-element ulp bound
+    # holds; the bounds are absolute, at the scale of the largest outputs.
     for s in (8, 32):
         diff = np.abs(outs[s] - outs[1])
-        assert diff.max() <= 2e-3 and diff.mean() <= 1e-4, f"splits {s} vs 1: max {diff.max()} mean {diff.mean()}"
+        assert diff.max() <= 2.0 ** -10 and diff.mean() <= 4.4e-5, \
+            f"splits {s} vs 1: max {diff.max()} mean {diff.mean()}"
     for s in (1, 32):
         step.splits = s
         step.attention()

@@ -1,10 +1,11 @@
 """The split-KV decode entry point that allocates nothing.
 
-Some callers cannot call cudaMalloc while they run the attention step: code
-being captured into a CUDA graph, serving runtimes that hand all device memory
-to their own allocator at start-up, and host environments that may not create
-device allocations at all. For them libdsa keeps the split partials in a fixed
-device scratch array instead of a caller workspace. These checks call that
+Some callers may not call cudaMalloc while they run the attention step:
+serving runtimes that hand all device memory to their own allocator at
+start-up and forbid later allocations, and host environments (plugins,
+sandboxed runtimes) that may not create device allocations at all. For them
+libdsa keeps the split partials in a fixed device scratch array instead of a
+caller workspace. These checks call that
 entry point through the C ABI twice in a row and compare each result with the
 workspace-based entry point on the same inputs. This file sorts last so that a
 stop-at-first-failure run has already run every other test.
