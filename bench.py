@@ -8,9 +8,13 @@ tokens each, 64x128 fp8 indexer, top-2048, 128-head 576/512 MLA). Prints one
 JSON line. `value` is decode tokens/s over the device-timed step with inputs
 resident in HBM and L2 flushed between steps; `e2e` repeats it through the
 public API with per-step inputs copied from pinned host memory and the output
-read back. `kernels` times each phase alone, `roofline` relates the dominant
-one to the HBM peak, `producer` times the key-cache writer (outside the step)
-and `cpu_baseline` the oracle on a bounded sample of the workload's tokens.
+read back. Times are medians over the timed steps (p10 / p90 beside them).
+`kernels` times each phase alone (medians; their sum must stay within 1.3x of
+the step median), `roofline` relates the dominant one to its peak (HBM at
+decode, the e4m3 or bf16 tensor peak at prefill), `workloads` repeats the
+measurement for the other four workloads (the long-context decode at 1, 8 and
+32 KV splits), `producer` times the key-cache writer (outside the step) and
+`cpu_baseline` the oracle on a bounded sample of the workload's tokens.
 Under torchrun every rank runs an independent replica (the step has no
 exchange), ranks are timed with a barrier and the max is taken.
 """
@@ -47,6 +51,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clock-load", action="store_true", help="skip the one-second load before the timed steps")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="time only --workload (by default the other workloads are timed too and reported under "
+                         "'workloads')")
     ap.add_argument("--oracle-seconds", type=int, default=0, metavar="N",
                     help="print the oracle's seconds for N evenly spaced query tokens of the workload and exit (no GPU)")
     return ap.parse_args()
@@ -240,6 +247,63 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def pct(xs, q):
+    return float(np.percentile(np.asarray(xs, dtype=np.float64), q))
+
+
+def summary(xs):
+    """Median and 10th / 90th percentiles of a list of milliseconds."""
+    return {"ms": pct(xs, 50), "p10_ms": pct(xs, 10), "p90_ms": pct(xs, 90)}
+
+
+def fp8_peak_tflops(peaks_doc):
+    """Dense e4m3 tensor peak: twice the measured bf16 burst (the nominal
+    fp8:bf16 ratio of this part; only bf16 is measured)."""
+    if peaks_doc and peaks_doc.get("bf16_tflops"):
+        return 2.0 * float(peaks_doc["bf16_tflops"]), "2 x measured bf16 burst (nominal fp8:bf16 ratio)"
+    return 2.0 * FALLBACK_BF16_TFLOPS, "2 x fallback bf16 (nominal fp8:bf16 ratio)"
+
+
+def bf16_peak_tflops(peaks_doc):
+    if peaks_doc and peaks_doc.get("bf16_tflops"):
+        return float(peaks_doc["bf16_tflops"]), "measured bf16 burst"
+    return FALLBACK_BF16_TFLOPS, "fallback bf16"
+
+
+def kernel_table(wl, phase_ms, alg, peaks_doc):
+    """Per-kernel achieved rate against its roofline: HBM bytes for the decode
+    shapes, tensor-core flops for the prefill indexer (e4m3) and prefill
+    attention (bf16)."""
+    hbm, _, _ = load_peaks()
+    prefill = wl.max_q_len > 2
+    fp8, fp8_src = fp8_peak_tflops(peaks_doc)
+    bf16, bf16_src = bf16_peak_tflops(peaks_doc)
+    rows = {
+        "indexer_logits": (alg["indexer"], alg["flops_indexer"], fp8, fp8_src),
+        "topk": (alg["topk"], 0, None, None),
+        "sparse_mla": (alg["attention"], alg["flops_attention"], bf16, bf16_src),
+    }
+    out = {}
+    for name, (nbytes, flops, tpeak, tsrc) in rows.items():
+        st = phase_ms[name]
+        sec = st["ms"] / 1e3
+        d = dict(st)
+        d["bytes"] = int(nbytes)
+        d["GBps"] = nbytes / sec / 1e9
+        d["hbm_frac"] = d["GBps"] / hbm
+        if flops:
+            d["flops"] = int(flops)
+            d["TFLOPs"] = flops / sec / 1e12
+            d["tensor_frac"] = d["TFLOPs"] / tpeak
+            d["tensor_peak"] = tpeak
+            d["tensor_peak_source"] = tsrc
+        tensor_bound = prefill and name != "topk"
+        d["bound"] = "tensor" if tensor_bound else "hbm"
+        d["frac"] = d["tensor_frac"] if tensor_bound else d["hbm_frac"]
+        out[name] = d
+    return out
+
+
 def main():
     args = parse()
     rank, world, local = dist_info()
@@ -285,12 +349,57 @@ def main():
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(max(3, args.warmup)):
-        step.run()
-    torch.cuda.synchronize()
-    assert int(step.dev_status.item()) == 0, "device status bits set during warm-up"
-    assert torch.isfinite(step.out.float()).all(), "non-finite output"
+    def warm(st, n):
+        for _ in range(max(3, n)):
+            st.run()
+        torch.cuda.synchronize()
+        assert int(st.dev_status.item()) == 0, "device status bits set during warm-up"
+        assert torch.isfinite(st.out.float()).all(), "non-finite output"
 
+    def time_steps(st, n):
+        # events only at step boundaries, so that nothing sits between the
+        # step's kernels (each is launched as a programmatic dependent of the
+        # one before); L2 flushed before every step
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        barrier()
+        for k in range(n):
+            flush_l2()
+            ev[k][0].record(stream)
+            st.run()
+            ev[k][1].record(stream)
+        barrier()
+        return [e[0].elapsed_time(e[1]) for e in ev]
+
+    def time_phases(st, n):
+        # each phase timed alone after its own L2 flush (its inputs are the
+        # previous phase's outputs, already in place)
+        evb = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n)]
+        for k in range(n):
+            e = evb[k]
+            for ph, fn in enumerate((st.indexer, st.topk, st.attention)):
+                flush_l2()
+                e[2 * ph].record(stream)
+                fn()
+                e[2 * ph + 1].record(stream)
+        barrier()
+        return {name: summary([evb[k][2 * ph].elapsed_time(evb[k][2 * ph + 1]) for k in range(n)])
+                for ph, name in enumerate(("indexer_logits", "topk", "sparse_mla"))}
+
+    def phases_consistent(st, t_step_ms, n):
+        """Phase medians whose sum is within 1.3x of the step median (each phase
+        alone pays its own launch and ramp, the chained step does not); one
+        re-measurement, then a hard failure."""
+        for _ in range(2):
+            ph = time_phases(st, n)
+            total = sum(v["ms"] for v in ph.values())
+            if total <= 1.3 * t_step_ms:
+                return ph, total
+        raise SystemExit(f"bench: phase medians sum to {total:.4f} ms, more than 1.3 x the step median "
+                         f"{t_step_ms:.4f} ms: the breakdown does not describe the step")
+
+    peak, peak_kind, peaks_doc = load_peaks()
+
+    warm(step, args.warmup)
     # clocks: sampler runs through a one-second sustained load and the timed steps
     sampler = ClockSampler(local)
     sampler.start()
@@ -301,36 +410,14 @@ def main():
         torch.cuda.synchronize()
 
     K = args.steps
-    # the timed steps: events only at step boundaries, so that nothing sits
-    # between the step's kernels (each is launched as a programmatic
-    # dependent of the one before)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    barrier()
     wall0 = time.perf_counter()
-    for k in range(K):
-        flush_l2()  # between steps: L2 holds nothing of the inputs, and nothing dirty
-        ev[k][0].record(stream)
-        step.run()
-        ev[k][1].record(stream)
-    barrier()
+    t_step = time_steps(step, K)
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
-    t_step = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
-    # per-kernel breakdown: each phase timed on its own, after its own L2
-    # flush (its inputs are the previous phase's outputs, already in place)
+    step_stats = summary(t_step)
     Kb = max(5, min(K, 50))
-    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(Kb)]
-    for k in range(Kb):
-        e = evb[k]
-        for ph, fn in enumerate((step.indexer, step.topk, step.attention)):
-            flush_l2()
-            e[2 * ph].record(stream)
-            fn()
-            e[2 * ph + 1].record(stream)
-    barrier()
-    t_idx = [evb[k][0].elapsed_time(evb[k][1]) for k in range(Kb)]
-    t_topk = [evb[k][2].elapsed_time(evb[k][3]) for k in range(Kb)]
-    t_att = [evb[k][4].elapsed_time(evb[k][5]) for k in range(Kb)]
+    phase_ms, phase_sum = phases_consistent(step, step_stats["ms"], Kb)
+
     # producer side, not part of the step: the new tokens' indexer keys
     # quantised into a scratch copy of the key cache
     from deepseek_sparse_attention_fp8_gb300 import api
@@ -346,11 +433,11 @@ def main():
                                           dev_status=step.dev_status)
         evp[k][1].record(stream)
     barrier()
-    t_prod = [evp[k][0].elapsed_time(evp[k][1]) for k in range(Kb)]
+    t_prod = summary([evp[k][0].elapsed_time(evp[k][1]) for k in range(Kb)])
     del k_scratch
     from deepseek_sparse_attention_fp8_gb300.replicas import aggregate
 
-    ms, _, value = aggregate(float(np.mean(t_step)), wl.T, step.device)
+    ms, _, value = aggregate(step_stats["ms"], wl.T, step.device)
 
     # warm-L2 (no flush) for context
     ew = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -383,50 +470,86 @@ def main():
             host_out.copy_(step.outputs, non_blocking=True)
             eve[k][1].record(stream)
         barrier()
-        ms_e2e, _, v_e2e = aggregate(float(np.mean([e[0].elapsed_time(e[1]) for e in eve])), wl.T, step.device)
+        e2e_stats = summary([e[0].elapsed_time(e[1]) for e in eve])
+        ms_e2e, _, v_e2e = aggregate(e2e_stats["ms"], wl.T, step.device)
         e2e = {"value": v_e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e}
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e, "p10_ms": e2e_stats["p10_ms"],
+               "p90_ms": e2e_stats["p90_ms"]}
 
     alg = algorithmic_bytes(wl, step.topk_idx.cpu().numpy())
-    peak, peak_kind, _ = load_peaks()
-    kern = {
-        "indexer_logits": {"ms": float(np.mean(t_idx)), "bytes": alg["indexer"]},
-        "topk": {"ms": float(np.mean(t_topk)), "bytes": alg["topk"]},
-        "sparse_mla_decode": {"ms": float(np.mean(t_att)), "bytes": alg["attention"],
-                              "flops": alg["flops_attention"]},
-    }
-    for k_, v in kern.items():
-        v["GBps"] = v["bytes"] / (v["ms"] / 1e3) / 1e9
-        v["frac"] = v["GBps"] / peak
+    kern = kernel_table(wl, phase_ms, alg, peaks_doc)
     # bf16 keys read, codes and scales written
     prod_bytes = wl.T * (wl.Di * 2 + wl.Di + 4)
-    producer = {"indexer_k_quant_and_cache": {"ms": float(np.mean(t_prod)), "bytes": prod_bytes,
-                                              "GBps": prod_bytes / (float(np.mean(t_prod)) / 1e3) / 1e9}}
+    producer = {"indexer_k_quant_and_cache": dict(t_prod, bytes=prod_bytes,
+                                                  GBps=prod_bytes / (t_prod["ms"] / 1e3) / 1e9)}
     producer["indexer_k_quant_and_cache"]["frac"] = producer["indexer_k_quant_and_cache"]["GBps"] / peak
     dom = max(kern, key=lambda k_: kern[k_]["ms"])
     traffic = load_traffic(dom, wl.name)
     step_bytes = alg["indexer"] + alg["topk"] + alg["attention"]
+    launches_per_step = step.kernel_launches()
+    splits_used = step.splits
+    del step
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": ms, "p10_ms": step_stats["p10_ms"], "p90_ms": step_stats["p90_ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3+bf16", "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "context": int(wl.seq_lens.max()),
                    "index_topk": wl.index_topk, "Hi": wl.Hi, "Di": wl.Di, "H": wl.H, "Dk": wl.Dk, "Dv": wl.Dv,
-                   "block_size": wl.block_size, "num_kv_splits": step.splits,
-                   "l2": "flushed between steps (256 MiB write + 256 MiB read)", "parallelism": "replicas" if world > 1 else "1 GPU"},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["GBps"], "peak": peak, "unit": "GB/s",
+                   "block_size": wl.block_size, "num_kv_splits": splits_used,
+                   "l2": "flushed between steps (256 MiB write + 256 MiB read)",
+                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "roofline": {"bound": kern[dom]["bound"], "kernel": dom,
+                     "achieved": kern[dom]["GBps"] if kern[dom]["bound"] == "hbm" else kern[dom]["TFLOPs"],
+                     "peak": peak if kern[dom]["bound"] == "hbm" else kern[dom]["tensor_peak"],
+                     "unit": "GB/s" if kern[dom]["bound"] == "hbm" else "TFLOP/s",
                      "frac": kern[dom]["frac"], "peak_source": peak_kind, "traffic": traffic,
                      "step_GBps": step_bytes / (ms / 1e3) / 1e9, "step_frac": step_bytes / (ms / 1e3) / 1e9 / peak},
         "kernels": kern,
+        "phase_sum_ms": phase_sum,
         "producer": producer,
         "warm_l2_ms_per_step": ms_warm,
-        "gpu_launches": step.kernel_launches() * K,
+        "gpu_launches": launches_per_step * K,
         "clocks": clocks,
         "wall_s": wall,
     }
     if e2e is not None:
         line["e2e"] = e2e
+
+    # the other workloads, each measured the same way (median of flushed
+    # steps, phases alone), on rank 0 at N=1 only
+    if world == 1 and not args.no_other_workloads:
+        others = {}
+        for name, splits_list in OTHER_WORKLOADS:
+            if name == wl.name:
+                continue
+            owl = make_workload(name)
+            for sp in splits_list:
+                ost = DsaStep(owl, device=step_device(local), num_kv_splits=sp)
+                warm(ost, 3)
+                n = max(5, min(K, 30))
+                ts = summary(time_steps(ost, n))
+                oph, osum = phases_consistent(ost, ts["ms"], max(5, min(n, 10)))
+                oalg = algorithmic_bytes(owl, ost.topk_idx.cpu().numpy())
+                okern = kernel_table(owl, oph, oalg, peaks_doc)
+                odom = max(okern, key=lambda k_: okern[k_]["ms"])
+                obytes = oalg["indexer"] + oalg["topk"] + oalg["attention"]
+                key = name if len(splits_list) == 1 else f"{name}_splits{sp}"
+                others[key] = {
+                    "config": {"workload": name, "B": owl.B, "T": owl.T, "context": int(owl.seq_lens.max()),
+                               "index_topk": owl.index_topk, "num_kv_splits": ost.splits,
+                               "prefill": bool(ost.prefill)},
+                    "value": owl.T / (ts["ms"] / 1e3), "unit": "tokens/s", "steps": n, **ts,
+                    "step_GBps": obytes / (ts["ms"] / 1e3) / 1e9,
+                    "step_frac": obytes / (ts["ms"] / 1e3) / 1e9 / peak,
+                    "dominant": odom, "kernels": okern, "phase_sum_ms": osum,
+                    "traffic": load_traffic(odom, name),
+                }
+                del ost
+                torch.cuda.empty_cache()
+        line["workloads"] = others
+
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rows, sec, busy = oracle_timed(wl)
         sec1 = oracle_one_thread_seconds(wl.name, len(rows))
@@ -439,6 +562,20 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def step_device(local):
+    return f"cuda:{local}"
+
+
+# Workloads measured beside the headline one: (name, split counts); the
+# long-context decode runs at the three split counts its parity test forces.
+OTHER_WORKLOADS = (
+    ("decode_b32_l8192", (0,)),
+    ("decode_b8_l131072", (1, 8, 32)),
+    ("prefill_4096_of_65536", (0,)),
+    ("mixed_b64_mtp2", (0,)),
+)
 
 
 def load_traffic(kernel, workload):
