@@ -56,6 +56,11 @@ class Workload:
     k_cache: np.ndarray
     q: np.ndarray
     kv_cache: np.ndarray
+    kv_cache_fp8: np.ndarray | None = None  # uint8 [num_blocks, block_size, 656] when drawn
+
+    @property
+    def kv_row_bytes_fp8(self) -> int:
+        return self.Dv + 4 * (self.Dv // 128) + 2 * (self.Dk - self.Dv)
 
     @property
     def max_q_len(self) -> int:
@@ -93,10 +98,11 @@ def _e4m3_codes(x: np.ndarray) -> np.ndarray:
 
 def make_workload(name: str, seed: int | None = None, *, B: int | None = None, L=None, q_len: int | None = None,
                   index_topk: int | None = None, ld_pad: int = 128, lens=None, block_size: int = 64,
-                  q_std: float = 1.0) -> Workload:
+                  q_std: float = 1.0, kv_fp8: bool = False) -> Workload:
     """Build one of the named workloads (optionally overriding a few sizes
     for smaller parity cases). `lens` gives explicit per-request lengths;
-    `q_std` the standard deviation of the MLA queries (1 in every workload)."""
+    `q_std` the standard deviation of the MLA queries (1 in every workload);
+    `kv_fp8` also lays the latent rows out as an fp8 latent cache."""
     spec = dict(WORKLOADS[name])
     if B is not None:
         spec["B"] = B
@@ -169,6 +175,30 @@ def make_workload(name: str, seed: int | None = None, *, B: int | None = None, L
         kv_cache[c0:c1] = _bf16_bits(kv)
     kv_cache[~used] = 0x7FC0
 
+    kv_cache_fp8 = None
+    if kv_fp8:
+        # the same latent rows as an fp8 cache: per token, the Dv latent values
+        # as e4m3 codes in groups of 128 with one fp32 scale each (amax/448,
+        # codes from PyTorch's float8 cast), then the rope values' bf16 bits;
+        # unused blocks hold e4m3 NaN bytes
+        assert Dv % 128 == 0
+        ng = Dv // 128
+        row_bytes = Dv + 4 * ng + 2 * (Dk - Dv)
+        kv_cache_fp8 = np.full((num_blocks, bs, row_bytes), 0x7F, dtype=np.uint8)
+        for c0 in range(0, num_blocks, 1024):
+            c1 = min(num_blocks, c0 + 1024)
+            u = used[c0:c1]
+            lat = bf16_bits_to_float(kv_cache[c0:c1][u, :, :Dv]).reshape(-1, bs, ng, 128)
+            amax = np.abs(lat).max(axis=-1)
+            scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+            codes = _e4m3_codes(lat / scale[..., None]).reshape(-1, bs, Dv)
+            blk = np.empty((int(u.sum()), bs, row_bytes), dtype=np.uint8)
+            blk[:, :, :Dv] = codes
+            blk[:, :, Dv:Dv + 4 * ng] = np.ascontiguousarray(scale).view(np.uint8).reshape(-1, bs, 4 * ng)
+            blk[:, :, Dv + 4 * ng:] = np.ascontiguousarray(kv_cache[c0:c1][u, :, Dv:]).view(np.uint8).reshape(
+                -1, bs, 2 * (Dk - Dv))
+            kv_cache_fp8[c0:c1][u] = blk
+
     q_idx = _bf16_bits(rng.standard_normal((T, Hi, Di), dtype=np.float32))
     w = (rng.standard_normal((T, Hi), dtype=np.float32) / np.float32(math.sqrt(Hi))).astype(np.float32)
     q = _bf16_bits(rng.standard_normal((T, H, Dk), dtype=np.float32) * np.float32(q_std))
@@ -179,4 +209,5 @@ def make_workload(name: str, seed: int | None = None, *, B: int | None = None, L
     return Workload(name=name, B=Bn, T=T, Hi=Hi, Di=Di, H=H, Dk=Dk, Dv=Dv, index_topk=spec["topk"], block_size=bs,
                     softmax_scale=1.0 / math.sqrt(Dk), seq_lens=seq_lens, query_start_loc=qsl,
                     block_table=block_table, num_blocks=num_blocks, k_block_stride=k_block_stride,
-                    kv_block_stride=bs * Dk, ld=ld, q_idx=q_idx, w=w, k_cache=k_cache, q=q, kv_cache=kv_cache)
+                    kv_block_stride=bs * Dk, ld=ld, q_idx=q_idx, w=w, k_cache=k_cache, q=q, kv_cache=kv_cache,
+                    kv_cache_fp8=kv_cache_fp8)

@@ -16,6 +16,8 @@ float64 with numpy, one query token at a time:
   a4  merge of the split partials by online softmax
   and, on the producer side, the new tokens' indexer keys quantised into the
   paged fp8 key cache (indexer_k_quant_and_cache)
+  the fp8 variant of the latent cache: its row layout, the quantisation of new
+  latent rows into it, and its decoding (a3 then runs on the decoded rows)
 
 Sources (web pages; cited by title and section):
   [PR]     vLLM PR #38476, "[Feature] TRITON_MLA_SPARSE backend for SM8x/11x/12x
@@ -52,6 +54,13 @@ Readings where the pages are silent:
   * An empty selection gives output 0 and lse -inf.
   * Split j covers top-k slots [j*ceil(K/S), min(K, (j+1)*ceil(K/S))); a -1
     slot scores the -1e30 sentinel and carries weight 0.
+  * fp8 latent cache ([PR] Limitations and review thread: the FP8-KV sparse-MLA
+    backends of SM90+/SM12x parts; the pages print no layout). One token's row
+    holds its Dv latent values as e4m3 codes in groups of 128 with one fp32
+    scale per group (the q rule: amax/448, 1 when amax == 0), then its Dk - Dv
+    rope values unchanged in bf16: [Dv code bytes][Dv/128 fp32 scales]
+    [(Dk-Dv) bf16], 656 bytes at Dk = 576, Dv = 512. A decoded latent value is
+    e4m3(code) * scale of its group.
 """
 from __future__ import annotations
 
@@ -442,3 +451,90 @@ def dense_mla(q_t, kv_rows, softmax_scale, dv):
         for i in range(kv_rows.shape[0]):
             out[h] += (e[i] / z) * kv_rows[i, :dv]
     return out
+
+
+# ----------------------------------------------------------------------------
+# fp8 latent KV cache (the FP8-KV variant of a3)
+# ----------------------------------------------------------------------------
+
+MLA_FP8_GROUP = 128
+
+
+def mla_fp8_row_bytes(dk: int, dv: int) -> int:
+    """Bytes of one token's row: dv e4m3 codes, dv/128 fp32 scales, and the
+    dk - dv rope values in bf16 (656 at dk = 576, dv = 512)."""
+    return dv + 4 * (dv // MLA_FP8_GROUP) + 2 * (dk - dv)
+
+
+def _bf16_bits_of(values) -> np.ndarray:
+    """bf16 bit patterns of values that are bf16 already (exact)."""
+    v = np.asarray(values, dtype=np.float32)
+    bits = v.view(np.uint32)
+    assert np.all((bits & 0xFFFF) == 0), "rope values must be bf16 values"
+    return (bits >> 16).astype(np.uint16)
+
+
+def mla_fp8_quantize_rows(kv, dv):
+    """Rows [n, dk] of bf16 latent values -> their fp8 cache rows [n, bytes].
+
+    The latent part is quantised in groups of 128 with the rule of
+    quantize_groups; the rope part keeps its bf16 bits.
+    """
+    kv = np.asarray(kv, dtype=np.float32)
+    n, dk = kv.shape
+    assert dv % MLA_FP8_GROUP == 0
+    ng = dv // MLA_FP8_GROUP
+    codes, scales = quantize_groups(kv[:, :dv].reshape(n, ng, MLA_FP8_GROUP))
+    out = np.zeros((n, mla_fp8_row_bytes(dk, dv)), dtype=np.uint8)
+    out[:, :dv] = codes.reshape(n, dv)
+    out[:, dv:dv + 4 * ng] = np.ascontiguousarray(scales.astype(np.float32)).view(np.uint8).reshape(n, 4 * ng)
+    out[:, dv + 4 * ng:] = np.ascontiguousarray(_bf16_bits_of(kv[:, dv:])).view(np.uint8).reshape(n, 2 * (dk - dv))
+    return out
+
+
+def mla_fp8_decode_rows(rows, dk, dv):
+    """fp8 cache rows [..., bytes] -> latent rows [..., dk] in float64:
+    e4m3(code) * scale of the code's group for the first dv values, the bf16
+    rope values for the rest."""
+    rows = np.asarray(rows, dtype=np.uint8)
+    lead = rows.shape[:-1]
+    r = rows.reshape(-1, rows.shape[-1])
+    ng = dv // MLA_FP8_GROUP
+    scales = np.ascontiguousarray(r[:, dv:dv + 4 * ng]).view(np.float32).astype(np.float64)  # [n, ng]
+    lat = e4m3_decode(r[:, :dv]).reshape(-1, ng, MLA_FP8_GROUP) * scales[:, :, None]
+    rope_bits = np.ascontiguousarray(r[:, dv + 4 * ng:dv + 4 * ng + 2 * (dk - dv)]).view(np.uint16)
+    rope = (rope_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    out = np.concatenate([lat.reshape(-1, dv), rope], axis=1)
+    return out.reshape(lead + (dk,))
+
+
+def mla_kv_fp8_quant_and_cache(kv, kv_cache_fp8, block_table, seq_lens, query_start_loc, block_size, dv):
+    """Producer side of the fp8 latent cache: a copy of the cache
+    [num_blocks, block_size, row_bytes] with the T new tokens' latent rows
+    kv [T, dk] (bf16 values) quantised by mla_fp8_quantize_rows and stored at
+    the tokens' positions pos(t) (block block_table[b, pos // block_size],
+    row pos % block_size), as indexer_k_quant_and_cache places keys. A position
+    past the block-table row or a block id outside the cache skips the token.
+    """
+    kv = np.asarray(kv, dtype=np.float32)
+    T, dk = kv.shape
+    rows = mla_fp8_quantize_rows(kv, dv)
+    out = np.array(kv_cache_fp8, dtype=np.uint8, copy=True)
+    bt = np.asarray(block_table)
+    req, pos = token_positions(seq_lens, query_start_loc)
+    for t in range(T):
+        b, p = int(req[t]), int(pos[t])
+        if p < 0 or p >= bt.shape[1] * block_size:
+            continue
+        blk = int(bt[b, p // block_size])
+        if blk < 0 or blk >= out.shape[0]:
+            continue
+        out[blk, p % block_size] = rows[t]
+    return out
+
+
+def mla_fp8_decode_cache(kv_cache_fp8, dk, dv):
+    """The whole fp8 latent cache [num_blocks, block_size, bytes] decoded to
+    float64 rows [num_blocks, block_size, dk]; a3 on the fp8 cache is
+    sparse_mla / sparse_mla_split over these rows."""
+    return mla_fp8_decode_rows(kv_cache_fp8, dk, dv)
