@@ -41,6 +41,9 @@ _SIGS = {
     "dsa_indexer_k_quant_and_cache": ([_p, _i64, _i32, _i32, _p, _i64, _i32, _p, _i32, _p, _p, _i32, _i32, _p, _p],
                                       _i32),
     "dsa_topk_workspace_size": ([_i32, _i64, _i32], _sz),
+    "dsa_indexer_topk_workspace_size": ([_i32, _i64, _i32, _i32], _sz),
+    "dsa_indexer_topk": ([_p, _i64, _p, _p, _i64, _i32, _p, _i32, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i64,
+                          _i32, _i32, _p, _p, _sz, _p, _p], _i32),
     "dsa_topk": ([_p, _i64, _p, _p, _i32, _i32, _i32, _p, _p, _sz, _p], _i32),
     "sparse_mla_workspace_size": ([_i32, _i32, _i32, _i32], _sz),
     "sparse_mla_auto_splits": ([_i32, _i32, _i32, _i32], _i32),
@@ -52,7 +55,15 @@ _SIGS = {
                                          _i32, _f32, _i32, _p, _p, _p, _p], _i32),
     "sparse_mla_prefill": ([_p, _p, _i64, _i32, _p, _i32, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32,
                             _p, _p, _p, _p], _i32),
+    "sparse_mla_decode_fp8": ([_p, _p, _i64, _i32, _p, _i32, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                               _f32, _i32, _p, _p, _p, _sz, _p, _p], _i32),
+    "sparse_mla_prefill_fp8": ([_p, _p, _i64, _i32, _p, _i32, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                _f32, _p, _p, _p, _p], _i32),
+    "dsa_mla_kv_fp8_quant_and_cache": ([_p, _i64, _i32, _i32, _i32, _p, _i64, _i32, _p, _i32, _p, _p, _i32, _i32, _p,
+                                        _p], _i32),
 }
+
+MLA_FP8_ROW_BYTES = 656  # fp8 latent cache row at Dk = 576, Dv = 512
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(lib, _name)
     _fn.argtypes = _args
@@ -150,6 +161,39 @@ def dsa_indexer_logits(q_idx, w, k_cache, block_table, seq_lens, query_start_loc
                                 _stream(stream))
     _check(st, "dsa_indexer_logits")
     return logits
+
+
+def dsa_indexer_topk_workspace_size(T: int, max_seq_len: int, window: int, index_topk: int) -> int:
+    return int(lib.dsa_indexer_topk_workspace_size(T, max_seq_len, window, index_topk))
+
+
+def dsa_indexer_topk(q_idx, w, k_cache, block_table, seq_lens, query_start_loc, block_size, max_q_len, max_seq_len,
+                     window, index_topk, topk_idx=None, workspace=None, dev_status=None, stream=None):
+    """a1 + a2 over key windows of `window` keys (0 = one window): topk_idx
+    [T, index_topk] (int32), the exact top-k of the indexer logits, with a
+    logits buffer of [T, window] instead of [T, max_seq_len]."""
+    _need(q_idx, torch.bfloat16, "q_idx", 3)
+    _need(w, torch.float32, "w", 2)
+    _need(k_cache, torch.uint8, "k_cache", 2)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(query_start_loc, torch.int32, "query_start_loc", 1)
+    T, Hi, Di = q_idx.shape
+    if topk_idx is None:
+        topk_idx = torch.empty((T, index_topk), dtype=torch.int32, device=q_idx.device)
+    _need(topk_idx, torch.int32, "topk_idx", 2)
+    if dev_status is not None:
+        _need(dev_status, torch.int32, "dev_status")
+    need = dsa_indexer_topk_workspace_size(T, max_seq_len, window, index_topk)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_idx.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.dsa_indexer_topk(_ptr(q_idx), Hi * Di, _ptr(w), _ptr(k_cache), k_cache.shape[1], k_cache.shape[0],
+                              _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc),
+                              seq_lens.shape[0], T, Hi, Di, block_size, max_q_len, max_seq_len, window, index_topk,
+                              _ptr(topk_idx), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
+    _check(st, "dsa_indexer_topk")
+    return topk_idx
 
 
 def dsa_topk_workspace_size(T: int, ld: int, index_topk: int) -> int:
@@ -269,3 +313,75 @@ def header_functions():
     with open(_H) as f:
         text = f.read()
     return sorted(set(re.findall(r"^\s*(?:const char\*|dsa_status_t|size_t|int32_t)\s+(\w+)\s*\(", text, re.M)))
+
+
+def _mla_fp8_common(q, kv_cache, block_table, seq_lens, query_start_loc, topk_idx, out, lse, dev_status):
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv_cache, torch.uint8, "kv_cache", 3)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(query_start_loc, torch.int32, "query_start_loc", 1)
+    _need(topk_idx, torch.int32, "topk_idx", 2)
+    _need(out, torch.bfloat16, "out", 3)
+    if lse is not None:
+        _need(lse, torch.float32, "lse", 2)
+    if dev_status is not None:
+        _need(dev_status, torch.int32, "dev_status")
+    num_blocks, block_size, row_bytes = kv_cache.shape
+    T, H, Dk = q.shape
+    return num_blocks, block_size, row_bytes, T, H, Dk
+
+
+def sparse_mla_decode_fp8(q, kv_cache, block_table, seq_lens, query_start_loc, topk_idx, softmax_scale, dv, out,
+                          lse=None, num_kv_splits=0, workspace=None, dev_status=None, stream=None):
+    """a3 + a4 over the fp8 latent cache kv_cache [blocks, block_size, 656] (uint8)."""
+    num_blocks, block_size, rb, T, H, Dk = _mla_fp8_common(q, kv_cache, block_table, seq_lens, query_start_loc,
+                                                           topk_idx, out, lse, dev_status)
+    K = topk_idx.shape[1]
+    splits = sparse_mla_num_splits(T, H, dv, K, num_kv_splits)
+    need = sparse_mla_workspace_size(T, H, dv, splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.sparse_mla_decode_fp8(_ptr(q), _ptr(kv_cache), block_size * rb, num_blocks, _ptr(block_table),
+                                   block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc), _ptr(topk_idx),
+                                   seq_lens.shape[0], T, H, Dk, dv, K, block_size, softmax_scale, num_kv_splits,
+                                   _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
+    _check(st, "sparse_mla_decode_fp8")
+    return out
+
+
+def sparse_mla_prefill_fp8(q, kv_cache, block_table, seq_lens, query_start_loc, topk_idx, softmax_scale, dv, out,
+                           lse=None, dev_status=None, stream=None):
+    """a3 single pass over the fp8 latent cache."""
+    num_blocks, block_size, rb, T, H, Dk = _mla_fp8_common(q, kv_cache, block_table, seq_lens, query_start_loc,
+                                                           topk_idx, out, lse, dev_status)
+    K = topk_idx.shape[1]
+    st = lib.sparse_mla_prefill_fp8(_ptr(q), _ptr(kv_cache), block_size * rb, num_blocks, _ptr(block_table),
+                                    block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc), _ptr(topk_idx),
+                                    seq_lens.shape[0], T, H, Dk, dv, K, block_size, softmax_scale, _ptr(out), _ptr(lse),
+                                    _ptr(dev_status), _stream(stream))
+    _check(st, "sparse_mla_prefill_fp8")
+    return out
+
+
+def dsa_mla_kv_fp8_quant_and_cache(kv, kv_cache, block_table, seq_lens, query_start_loc, block_size, dv=512,
+                                   dev_status=None, stream=None):
+    """Quantises the new tokens' latent rows kv [T, Dk] (bf16) into the fp8
+    latent cache kv_cache [num_blocks, block_size, 656] (uint8) in place."""
+    _need(kv, torch.bfloat16, "kv", 2)
+    _need(kv_cache, torch.uint8, "kv_cache", 3)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(query_start_loc, torch.int32, "query_start_loc", 1)
+    if dev_status is not None:
+        _need(dev_status, torch.int32, "dev_status")
+    T, Dk = kv.shape
+    nb, bs, rb = kv_cache.shape
+    if bs != block_size:
+        raise ValueError("kv_cache's second dim must be block_size")
+    st = lib.dsa_mla_kv_fp8_quant_and_cache(_ptr(kv), Dk, T, Dk, dv, _ptr(kv_cache), bs * rb, nb, _ptr(block_table),
+                                            block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc),
+                                            seq_lens.shape[0], block_size, _ptr(dev_status), _stream(stream))
+    _check(st, "dsa_mla_kv_fp8_quant_and_cache")
+    return kv_cache

@@ -26,9 +26,11 @@
 //                     accumulator in tensor memory.
 // Warp roles: 8 softmax/epilogue warps, 4 producer warps (TMA), 1 MMA warp.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <cmath>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -50,9 +52,7 @@ constexpr float kRescaleThreshold = 8.f;  // log2 units
 constexpr int kMaxSlots = 2048;           // top-k slots one CTA (one split) may cover
 constexpr int kXBufs = 2;                 // score-exchange buffers, one per softmax group
 constexpr long long kWaitLimitCycles = 2000000000ll;
-constexpr int kQStage = 2;  // q is staged in KV stages 2 and 3
 static_assert(kMaxSlots <= 256 * 8, "the softmax warps resolve all slots in one pass");
-static_assert(kQStage + 2 <= kStages, "q staging needs two KV stages");
 constexpr int kXRow = 64 * 4;             // bytes of one row's 64 fp32 scores in an exchange buffer
 constexpr int kXChunk = 128 * 16;         // stride of a 16-byte chunk column (128 rows) in an exchange buffer
 
@@ -78,22 +78,42 @@ struct MlaCfg<80, 64> {
   static constexpr int kRopeX = 0;
 };
 
-template <int DK, int DV>
+// Shared-memory layout. F8: the latent cache is fp8 (e4m3 codes in groups of
+// 128 dims with an fp32 scale each, then the rope dims in bf16); its codes
+// and scales are gathered into raw stages and dequantised by the producer
+// warps into the bf16 operand stages the MMAs read.
+template <int DK, int DV, bool F8>
 struct MlaSmem {
   using C = MlaCfg<DK, DV>;
+  static constexpr int kBStages = F8 ? 3 : kStages;  // bf16 operand stages
+  static constexpr int kRStages = F8 ? 2 : 0;        // raw fp8 stages (codes + scales)
+  static constexpr int kQStage = F8 ? 1 : 2;         // q is staged in bf16 stages kQStage, kQStage + 1
   static constexpr int kKvKb = kTileKeys * 128;  // one 64-dim K-block of a KV tile
   static constexpr int kKvHalf = C::kMaxNkb * kKvKb;  // the rope half-block: 64 keys x 64 B (SWIZZLE_64B)
   static constexpr int kKvStage = kKvHalf + (C::kRopeHalf ? kTileKeys * 64 : 0);
   static constexpr int kQHalf = C::kRopeHalf ? 128 * 64 : 0;  // q's rope half: 128 heads x 64 B
+  static constexpr int kRawCodes = kTileKeys * 256;  // this CTA's 256 codes of each key
+  // then the keys' four group scales (16 bytes a key); a 4-row gather writes
+  // 64 bytes, and tensor copies need 128-byte aligned destinations, so each
+  // group of 4 keys takes a 128-byte slot
+  static constexpr int kRawScaleSlot = 128;
+  static constexpr int kRawStage = kRawCodes + (kTileKeys / 4) * kRawScaleSlot;
   static constexpr int kKv = 0;
-  static constexpr int kX = kKv + kStages * kKvStage;
+  static constexpr int kRaw = kKv + kBStages * kKvStage;
+  static constexpr int kX = kRaw + kRStages * kRawStage;  // [kKv, kX) is idle at write-out
   static constexpr int kXBuf = 128 * kXRow;
   static constexpr int kRow = kX + (C::kPair ? kXBufs * kXBuf : 0);
   static constexpr int kLive = kRow + kMaxSlots * 4;
-  static constexpr int kCoord = kLive + kStages * kTileKeys;
-  static constexpr int kRed = kCoord + kStages * kTileKeys * 4;
+  static constexpr int kCoordStages = F8 ? kRStages : kBStages;
+  static constexpr int kCoord = kLive + kBStages * 4 * 2;
+  static constexpr int kRed = kCoord + kCoordStages * kTileKeys * 4;
   static constexpr int kTotal = kRed + 6 * 128 * 4 + 1024;
   static_assert(C::kMaxNkb * 16384 + kQHalf <= 2 * kKvStage, "q staging does not fit in two KV stages");
+  static_assert(kQStage + 2 <= kBStages, "q staging needs two bf16 stages");
+  static_assert(!F8 || (C::kPair && C::kNkb == 4), "the fp8 cache is read by the paired 576/512 kernel only");
+  // every TMA destination is 128-byte aligned (stages are 1024-byte multiples)
+  static_assert(kKvStage % 1024 == 0 && kRawStage % 1024 == 0 && kRawCodes % 128 == 0 && kRaw % 1024 == 0,
+                "TMA destinations must stay 128-byte aligned");
 };
 
 struct MlaParams {
@@ -126,14 +146,27 @@ __device__ __forceinline__ int find_request(const int32_t* qsl, int B, int t) {
   return lo;
 }
 
-template <int DK, int DV>
+// e4m3 pair (low byte = first value) -> two bf16 of code * scale, packed
+// with the first value in the low half.
+__device__ __forceinline__ uint32_t dequant_e4m3x2(uint32_t two, float sc) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(two)));
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  return pack_bf16(f.x * sc, f.y * sc);
+}
+
+template <int DK, int DV, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_constant__ MlaParams p,
                                                                  const __grid_constant__ CUtensorMap qmap,
                                                                  const __grid_constant__ CUtensorMap kvmap,
                                                                  const __grid_constant__ CUtensorMap qmap64,
-                                                                 const __grid_constant__ CUtensorMap kvmap64) {
+                                                                 const __grid_constant__ CUtensorMap kvmap64,
+                                                                 const __grid_constant__ CUtensorMap scmap) {
+  // F8: kvmap = the cache rows' code bytes (256-byte boxes), kvmap64 = their
+  // rope dims (bf16, 64-byte boxes, SWIZZLE_64B), scmap = their 16 scale bytes
   using C = MlaCfg<DK, DV>;
-  using L = MlaSmem<DK, DV>;
+  using L = MlaSmem<DK, DV, F8>;
+  constexpr int kBS = L::kBStages;
   constexpr int kSplitDv = C::kPair ? 2 : 1;
   // tensor-memory columns: S (fp32), O (fp32), Q (bf16 pairs), P (bf16 pairs)
   constexpr uint32_t kColS = 0, kColO = kTileKeys, kColQ = kTileKeys + C::kDvc;
@@ -143,6 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t kv_full[kStages], kv_empty[kStages], x_full[kXBufs], x_empty[kXBufs];
+  // F8: per raw stage and producer warp, the TMA completion of that warp's
+  // codes + scales
+  __shared__ uint64_t raw_full[2][4];
   // s_full, o_done and m_bar come in pairs indexed by tile parity, so each
   // softmax group waits on phases of its own tiles only
   __shared__ uint64_t s_full[2], s_free, p_full, o_done[2], o_final, q_full, q_ready, rows_ready, m_bar[2], epi_bar;
@@ -157,7 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   const int t = blockIdx.x / (kSplitDv * p.splits);
   const int kb0 = r * C::kNkb;                     // first K-block (64 dims) this CTA owns
   constexpr int nkb = C::kNkb;                     // K-blocks this CTA owns
-  const int rope_x = C::kRopeX + 32 * r;           // its rope half (dims), when there is one
+  const int rope_x = C::kRopeX + 32 * r;           // its rope half (dims of q), when there is one
+  // ... and the same dims in a cache row: bf16 element 512 + 32 r of a bf16
+  // row; in an fp8 row the rope follows DV code bytes and DV / 128 scales
+  const int rope_kv = F8 ? (DV + 4 * (DV / 128)) / 2 + 32 * r : rope_x;
 
   uint8_t* kv_sm = smem + L::kKv;
   uint8_t* x_sm = smem + L::kX;
@@ -167,8 +206,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 4);  // the four producer warps
+      // the four producer warps; F8: each arrives twice, when it issues the
+      // stage's rope gather (with its bytes) and when its keys are dequantised
+      mbar_init(&kv_full[s], F8 ? 8 : 4);
       mbar_init(&kv_empty[s], 1);
+    }
+    if constexpr (F8) {
+      for (int w = 0; w < 4; ++w)
+        for (int s = 0; s < 2; ++s) mbar_init(&raw_full[s][w], 1);
     }
     for (int s = 0; s < kXBufs; ++s) {
       mbar_init(&x_full[s], 1);   // local expect_tx; the peer's st.async deliver the bytes
@@ -203,23 +248,27 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tmem = tmem_holder;
 
-  // Launched as a programmatic dependent: everything above touches no global
-  // memory; from here on the previous kernel's results are visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int slot0 = j * p.per_split;
-  const int n_slots = max(0, min(p.K, slot0 + p.per_split) - slot0);
-  // the softmax warps load their top-k slots first; meanwhile the request of
-  // token t (the last b with query_start_loc[b] <= t) is found in one round of
-  // loads when the batch has at most kThreads requests
-  const int32_t* idx_row = p.topk + static_cast<int64_t>(t) * p.K + slot0;
-  int idx[8];
-  if (warp < 8) {
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int sl = u * 256 + tid;
-      idx[u] = sl < n_slots ? __ldg(idx_row + sl) : -1;
+  // Launched as a programmatic dependent of the top-k. q, query_start_loc and
+  // seq_lens are inputs of the step that no kernel of the library writes, so
+  // this CTA's q K-blocks (by TMA, into KV stages kQStage..., which tiles 0
+  // and 1 leave untouched) and the token's request are fetched before the
+  // wait, overlapping the top-k's tail; the top-k slots are read after it.
+  uint8_t* q_stage = kv_sm + L::kQStage * L::kKvStage;
+  if (tid == kProdWarp0 * 32) {  // first producer thread
+    prefetch_tmap(&qmap);
+    prefetch_tmap(&kvmap);
+    if constexpr (C::kRopeHalf) {
+      prefetch_tmap(&qmap64);
+      prefetch_tmap(&kvmap64);
     }
+    if constexpr (F8) prefetch_tmap(&scmap);
+    mbar_arrive_expect_tx(&q_full, nkb * 16384 + L::kQHalf);
+    for (int kb = 0; kb < nkb; ++kb)
+      tma_load_3d(smem_u32(q_stage + kb * 16384), &qmap, &q_full, (kb0 + kb) * 64, 0, t);
+    if constexpr (C::kRopeHalf) tma_load_3d(smem_u32(q_stage + nkb * 16384), &qmap64, &q_full, rope_x, 0, t);
   }
+  // the request of token t: the last b with query_start_loc[b] <= t, found in
+  // one round of loads when the batch has at most kThreads requests
   int b, q0, q1, sl_b;
   if (p.B <= kThreads) {
     const int qv = tid <= p.B ? __ldg(p.qsl + tid) : 0;
@@ -244,27 +293,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   }
   const int valid = static_cast<int>(valid64);
 
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the top-k's results are visible from here on
+  const int slot0 = j * p.per_split;
+  const int n_slots = max(0, min(p.K, slot0 + p.per_split) - slot0);
+  const int32_t* idx_row = p.topk + static_cast<int64_t>(t) * p.K + slot0;
+  int idx[8];
+  if (warp < 8) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int sl = u * 256 + tid;
+      idx[u] = sl < n_slots ? __ldg(idx_row + sl) : -1;
+    }
+  }
+
   auto abort_now = [&](void) {
     s_abort = 1;
     report(p.dev_status, DSA_DEVERR_TIMEOUT);
   };
 
-  // ---- prologue: this CTA's q K-blocks go by TMA into KV stages kQStage..,
-  // which tiles 0 and 1 leave untouched, so the producers start gathering as
-  // soon as the slots are resolved, while q moves on into tensor memory
-  uint8_t* q_stage = kv_sm + kQStage * L::kKvStage;
-  if (tid == kProdWarp0 * 32) {  // first producer thread
-    prefetch_tmap(&qmap);
-    prefetch_tmap(&kvmap);
-    if constexpr (C::kRopeHalf) {
-      prefetch_tmap(&qmap64);
-      prefetch_tmap(&kvmap64);
-    }
-    mbar_arrive_expect_tx(&q_full, nkb * 16384 + L::kQHalf);
-    for (int kb = 0; kb < nkb; ++kb)
-      tma_load_3d(smem_u32(q_stage + kb * 16384), &qmap, &q_full, (kb0 + kb) * 64, 0, t);
-    if constexpr (C::kRopeHalf) tma_load_3d(smem_u32(q_stage + nkb * 16384), &qmap64, &q_full, rope_x, 0, t);
-  }
   if (warp < 8) {
     // the split's top-k slots -> physical rows (-1: empty or invalid)
     const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
@@ -338,19 +384,126 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   if (!mbar_wait(&rows_ready, 0) && lane == 0) abort_now();
   const int n_tiles = s_abort ? 0 : (s_last_live + kTileKeys) / kTileKeys;
 
-  if (warp >= kProdWarp0 && warp < kMmaWarp) {
+  if (F8 && warp >= kProdWarp0 && warp < kMmaWarp) {
+    // ---------------- fp8 producer: 4 warps, 16 keys each. Codes + scales of
+    // tile i go by 4-row TMA gathers into raw stage i % 2 two tiles ahead;
+    // when bf16 stage i % 3 is free its rope half is gathered straight into
+    // it (the bytes counted on the stage's barrier, which the MMA waits for),
+    // the warp dequantises its 16 keys (code * group scale -> bf16, in the
+    // MMA's swizzled layout), hands its part of the stage to the MMA and
+    // gathers tile i + 2's codes.
+    const int pw = warp - kProdWarp0;
+    const int g = pw * 4 + (lane & 3);  // 4-row group a gathering lane issues
+    uint32_t live_bits0 = 0u, live_bits1 = 0u;  // live-key bits of the tiles in raw stages 0 and 1
+    int codes_issued = 0, codes_done = 0;
+    int open_stage = -1;  // a tile whose rope this warp gathered but whose stage it has not handed over
+    auto issue_codes = [&](int i) {
+      const int rst = i & 1;
+      bool live = false;
+      if (lane < 16) {
+        const int kr = pw * 16 + lane;
+        const int sl = i * kTileKeys + kr;
+        const int row = sl < n_slots ? row_sm[sl] : -1;
+        live = row >= 0;
+        coord_sm[rst * kTileKeys + kr] = live ? row : p.total_rows;  // out of range: zero fill
+      }
+      const uint32_t bits = __ballot_sync(0xFFFFFFFFu, live) & 0xFFFFu;
+      if (rst) live_bits1 = bits; else live_bits0 = bits;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&raw_full[rst][pw], 16 * (256 + 16));
+      __syncwarp();
+      const int* cs = coord_sm + rst * kTileKeys + 4 * g;
+      uint8_t* raw = smem + L::kRaw + rst * L::kRawStage;
+      if (lane < 4)
+        tma_gather4(smem_u32(raw + g * 4 * 256), &kvmap, &raw_full[rst][pw], 256 * r, cs[0], cs[1], cs[2], cs[3]);
+      else if (lane < 8)
+        tma_gather4(smem_u32(raw + L::kRawCodes + g * L::kRawScaleSlot), &scmap, &raw_full[rst][pw], DV, cs[0], cs[1],
+                    cs[2], cs[3]);
+      codes_issued = i + 1;
+    };
+    for (int i = 0; i < min(2, n_tiles); ++i) issue_codes(i);
+    for (int i = 0; i < n_tiles && !s_abort; ++i) {
+      const int bst = i % kBS, rst = i & 1;
+      if (i >= kBS && !mbar_wait(&kv_empty[bst], ((i / kBS) - 1) & 1)) {
+        if (lane == 0) abort_now();
+        break;
+      }
+      if (i == L::kQStage && !mbar_wait(&q_ready, 0)) {  // q has left its staging stages
+        if (lane == 0) abort_now();
+        break;
+      }
+      uint8_t* stage = kv_sm + bst * L::kKvStage;
+      // the rope half of this warp's keys, straight into the bf16 stage
+      if (lane == 0) mbar_arrive_expect_tx(&kv_full[bst], 16 * 64);
+      __syncwarp();
+      if (lane < 4) {
+        const int* cs = coord_sm + rst * kTileKeys + 4 * g;
+        tma_gather4(smem_u32(stage + L::kKvHalf + g * 256), &kvmap64, &kv_full[bst], rope_kv, cs[0], cs[1], cs[2],
+                    cs[3]);
+      }
+      open_stage = i;
+      if (!mbar_wait(&raw_full[rst][pw], (i >> 1) & 1)) {
+        if (lane == 0) abort_now();
+        break;
+      }
+      codes_done = i + 1;
+      {
+        // lane: key pw * 16 + lane / 2, group lane % 2 of this CTA's two
+        // 128-dim groups (K-blocks 2 grp, 2 grp + 1); 16 codes per step, the
+        // step order rotated by lane so that a quarter-warp's loads hit
+        // distinct banks
+        const int k = pw * 16 + (lane >> 1), grp = lane & 1;
+        const uint8_t* raw = smem + L::kRaw + rst * L::kRawStage;
+        const uint8_t* src = raw + k * 256 + grp * 128;
+        const float sc = *reinterpret_cast<const float*>(raw + L::kRawCodes + (k >> 2) * L::kRawScaleSlot +
+                                                         (k & 3) * 16 + (2 * r + grp) * 4);
+        uint8_t* dst = stage + (2 * grp) * L::kKvKb + k * 128;
+        const uint32_t sw = static_cast<uint32_t>(k & 7);
+#pragma unroll 2
+        for (int step = 0; step < 8; ++step) {
+          const int jj = (step + lane) & 7;  // dims 16 jj .. 16 jj + 15 of the group
+          const uint4 c = *reinterpret_cast<const uint4*>(src + jj * 16);
+          uint8_t* kb = dst + (jj >> 2) * L::kKvKb;
+          const uint32_t c0 = 2u * static_cast<uint32_t>(jj & 3);
+          *reinterpret_cast<uint4*>(kb + ((c0 ^ sw) << 4)) =
+              make_uint4(dequant_e4m3x2(c.x, sc), dequant_e4m3x2(c.x >> 16, sc), dequant_e4m3x2(c.y, sc),
+                         dequant_e4m3x2(c.y >> 16, sc));
+          *reinterpret_cast<uint4*>(kb + (((c0 + 1u) ^ sw) << 4)) =
+              make_uint4(dequant_e4m3x2(c.z, sc), dequant_e4m3x2(c.z >> 16, sc), dequant_e4m3x2(c.w, sc),
+                         dequant_e4m3x2(c.w >> 16, sc));
+        }
+      }
+      if (lane == 0) live_m[bst * 4 + pw] = static_cast<uint16_t>(rst ? live_bits1 : live_bits0);
+      fence_proxy_async_smem();  // the MMA reads the stage through the async proxy
+      __syncwarp();              // every lane is done with raw stage rst
+      if (lane == 0) mbar_arrive(&kv_full[bst]);
+      open_stage = -1;
+      if (i + 2 < n_tiles) issue_codes(i + 2);
+    }
+    if (s_abort) {
+      // let this warp's gathers in flight land before shared memory is given
+      // up: its codes on its own barriers; a rope gather by completing this
+      // warp's arrivals on the stage's barrier and waiting for the phase
+      for (int i = codes_done; i < codes_issued; ++i) mbar_wait(&raw_full[i & 1][pw], (i >> 1) & 1, 20000000ll);
+      if (open_stage >= 0) {
+        if (lane == 0) mbar_arrive(&kv_full[open_stage % kBS]);
+        mbar_wait(&kv_full[open_stage % kBS], (open_stage / kBS) & 1, 20000000ll);
+      }
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  } else if (warp >= kProdWarp0 && warp < kMmaWarp) {
     // ---------------- producer: 4 warps, 16 keys each; 4-row TMA gathers of
     // this CTA's K-blocks only
     const int pw = warp - kProdWarp0;
     const uint32_t tile_bytes = kTileKeys * (nkb * 128 + (C::kRopeHalf ? 64 : 0));
     int issued = 0;
     for (int i = 0; i < n_tiles && !s_abort; ++i) {
-      const int st = i % kStages;
-      if (i >= kStages && !mbar_wait(&kv_empty[st], ((i / kStages) - 1) & 1)) {
+      const int st = i % kBS;
+      if (i >= kBS && !mbar_wait(&kv_empty[st], ((i / kBS) - 1) & 1)) {
         if (lane == 0) abort_now();
         break;
       }
-      if (i == kQStage && !mbar_wait(&q_ready, 0)) {  // q has left its staging stages
+      if (i == L::kQStage && !mbar_wait(&q_ready, 0)) {  // q has left its staging stages
         if (lane == 0) abort_now();
         break;
       }
@@ -377,15 +530,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       } else if (C::kRopeHalf && lane < 4 * nkb + 4) {  // the rope half of the same 4-row groups
         const int g = pw * 4 + (lane & 3);
         const int* cs = coord_sm + st * kTileKeys + 4 * g;
-        tma_gather4(smem_u32(kv_sm + st * L::kKvStage + L::kKvHalf + g * 256), &kvmap64, &kv_full[st], rope_x, cs[0],
+        tma_gather4(smem_u32(kv_sm + st * L::kKvStage + L::kKvHalf + g * 256), &kvmap64, &kv_full[st], rope_kv, cs[0],
                     cs[1], cs[2], cs[3]);
       }
       issued = i + 1;
     }
     if (s_abort && pw == 0) {
       // let the gathers in flight land before shared memory is given up
-      for (int i = max(0, issued - kStages); i < issued; ++i)
-        mbar_wait(&kv_full[i % kStages], (i / kStages) & 1, 20000000ll);
+      for (int i = max(0, issued - kBS); i < issued; ++i)
+        mbar_wait(&kv_full[i % kBS], (i / kBS) & 1, 20000000ll);
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   } else if (warp == kMmaWarp) {
@@ -397,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     const uint32_t idesc_qk = idesc_bf16(128, kTileKeys, false, false);
     const uint32_t idesc_pv = idesc_bf16(128, C::kDvc, false, true);
     auto issue_qk = [&](int i) {  // this CTA's part of S = Q K^T
-      const int st = i % kStages;
+      const int st = i % kBS;
       // descriptors differ only in the start-address field (16-byte units)
       const uint64_t d0 = smem_desc(smem_u32(kv_sm + st * L::kKvStage), 16, 1024, kSwizzle128B);
 #pragma unroll
@@ -417,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
       mma_commit(&s_full[i & 1]);
     };
     auto issue_pv = [&](int i) {  // O += P V
-      const int st = i % kStages;
+      const int st = i % kBS;
       // value dims = this CTA's first K-blocks
       const uint64_t vd = smem_desc(smem_u32(kv_sm + st * L::kKvStage), L::kKvKb, 1024, kSwizzle128B);
       // A = P from tensor memory: 16 keys (8 columns of bf16 pairs) per MMA
@@ -434,8 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     while (np < n_tiles && !s_abort) {
       bool progressed = false;
       if (nq < n_tiles) {
-        const int st = nq % kStages;
-        bool ready = mbar_test_wait(&kv_full[st], (nq / kStages) & 1) &&
+        const int st = nq % kBS;
+        bool ready = mbar_test_wait(&kv_full[st], (nq / kBS) & 1) &&
                      (nq == 0 || mbar_test_wait(&s_free, (nq - 1) & 1));
         ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
         if (ready) {
@@ -490,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     float m_own = kNegSentinel, l_part = 0.f;  // l_part is expressed against m_own
     for (int i = g; i < n_tiles && !s_abort; i += 2) {
       const int u = i >> 1;  // tiles this group has finished
-      const int st = i % kStages;
+      const int st = i % kBS;
       float s[kTileKeys];
       if (!mbar_wait(&s_full[g], u & 1)) {
         if (lane == 0) abort_now();
@@ -553,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free);
       }
-      if (!mbar_wait(&kv_full[st], (i / kStages) & 1)) {  // orders the producers' live masks
+      if (!mbar_wait(&kv_full[st], (i / kBS) & 1)) {  // orders the producers' live masks
         if (lane == 0) abort_now();
         break;
       }
@@ -655,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     // warp stores its 32 rows as contiguous segments, 16 bytes per lane.
     constexpr int kHalf = C::kDvc / 2;
     constexpr int kPitch = kHalf * 4 + 16;  // staged row: fp32 or bf16 values + pad
-    static_assert(8 * 32 * kPitch <= kStages * L::kKvStage, "write-out staging does not fit");
+    static_assert(8 * 32 * kPitch <= L::kX, "write-out staging does not fit");
     const bool final_out = p.splits == 1;  // bf16 output, else fp32 partials
     uint8_t* stg = kv_sm + warp * 32 * kPitch;
     {
@@ -784,47 +937,75 @@ dsa_status_t launch_merge(const MlaParams& p, int Dv, float* lse, cudaStream_t s
   return DSA_OK;
 }
 
-FuncAttrOnce g_smem_big, g_smem_tiny;
+FuncAttrOnce g_smem_big, g_smem_tiny, g_smem_f8;
 
 int dv_split_for(int Dv) { return Dv == 512 ? 2 : 1; }
 
+// Bytes of one fp8 cache row: Dv codes, Dv / 128 fp32 scales, the rope in bf16.
+constexpr int fp8_row_bytes(int Dk, int Dv) { return Dv + 4 * (Dv / 128) + 2 * (Dk - Dv); }
+
 // q [T, H, Dk] as a 3-D tensor (box: 64 dims x 128 heads x 1 token) and the
-// latent cache as 2-D rows of Dk (box: 64 dims x 1 row, gathered 4 rows at a
-// time); both 128-byte swizzled to match the MMA operand layout.
-dsa_status_t launch_mla(const MlaParams& p, const void* q, const void* kv, int Dk, int Dv, cudaStream_t s) {
+// latent cache as 2-D rows (gathered 4 rows at a time). bf16 cache: boxes of
+// 64 dims (SWIZZLE_128B, the MMA operand layout) and 32 rope dims
+// (SWIZZLE_64B). fp8 cache (f8): 256 code bytes and 16 scale bytes (no
+// swizzle; dequantised by the kernel) and 32 rope dims (SWIZZLE_64B).
+dsa_status_t launch_mla(const MlaParams& p, const void* q, const void* kv, int Dk, int Dv, bool f8, cudaStream_t s) {
   const int64_t grid = static_cast<int64_t>(p.T) * p.splits * dv_split_for(Dv);
   if (grid > 0x7FFFFFFF) return fail(DSA_ERR_UNSUPPORTED, "sparse_mla: grid too large");
-  // q and the latent rows, each as 64-dim blocks (128-byte rows, SWIZZLE_128B)
-  // and, for the rope dims split between the two CTAs, as 32-dim half-blocks
-  // (64-byte rows, SWIZZLE_64B)
-  CUtensorMap qmap, kvmap, qmap64, kvmap64;
+  const uint64_t rows = static_cast<uint64_t>(std::max(p.total_rows, 1));
+  CUtensorMap qmap, kvmap, qmap64, kvmap64, scmap;
+  memset(&scmap, 0, sizeof(scmap));
   for (int half = 0; half < 2; ++half) {
     const uint32_t w = half ? 32 : 64;
     const CUtensorMapSwizzle sw = half ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
-    {
-      const uint64_t dims[3] = {static_cast<uint64_t>(Dk), static_cast<uint64_t>(p.H), static_cast<uint64_t>(p.T)};
-      const uint64_t strides[2] = {static_cast<uint64_t>(Dk) * 2, static_cast<uint64_t>(p.H) * Dk * 2};
-      const uint32_t box[3] = {w, 128, 1};
-      dsa_status_t st = make_tmap(half ? &qmap64 : &qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box, sw);
-      if (st != DSA_OK) return st;
-    }
-    {
-      const uint64_t dims[2] = {static_cast<uint64_t>(Dk), static_cast<uint64_t>(std::max(p.total_rows, 1))};
+    const uint64_t dims[3] = {static_cast<uint64_t>(Dk), static_cast<uint64_t>(p.H), static_cast<uint64_t>(p.T)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(Dk) * 2, static_cast<uint64_t>(p.H) * Dk * 2};
+    const uint32_t box[3] = {w, 128, 1};
+    dsa_status_t st = make_tmap(half ? &qmap64 : &qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box, sw);
+    if (st != DSA_OK) return st;
+  }
+  if (!f8) {
+    for (int half = 0; half < 2; ++half) {
+      const uint32_t w = half ? 32 : 64;
+      const CUtensorMapSwizzle sw = half ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+      const uint64_t dims[2] = {static_cast<uint64_t>(Dk), rows};
       const uint64_t strides[1] = {static_cast<uint64_t>(Dk) * 2};
       const uint32_t box[2] = {w, 1};
       dsa_status_t st = make_tmap(half ? &kvmap64 : &kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv, dims, strides, box, sw);
       if (st != DSA_OK) return st;
     }
+  } else {
+    const uint64_t rb = static_cast<uint64_t>(fp8_row_bytes(Dk, Dv));
+    {
+      const uint64_t dims[2] = {rb, rows};
+      const uint64_t strides[1] = {rb};
+      const uint32_t box_codes[2] = {256, 1}, box_scales[2] = {16, 1};
+      dsa_status_t st = make_tmap(&kvmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv, dims, strides, box_codes,
+                                  CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (st != DSA_OK) return st;
+      st = make_tmap(&scmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv, dims, strides, box_scales, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (st != DSA_OK) return st;
+    }
+    {
+      const uint64_t dims[2] = {rb / 2, rows};
+      const uint64_t strides[1] = {rb};
+      const uint32_t box[2] = {32, 1};
+      dsa_status_t st = make_tmap(&kvmap64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv, dims, strides, box,
+                                  CU_TENSOR_MAP_SWIZZLE_64B);
+      if (st != DSA_OK) return st;
+    }
   }
   dsa_status_t st;
   if (Dk == 576) {
-    st = allow_smem(sparse_mla_kernel<576, 512>, MlaSmem<576, 512>::kTotal, g_smem_big);
+    const int smem = f8 ? MlaSmem<576, 512, true>::kTotal : MlaSmem<576, 512, false>::kTotal;
+    st = f8 ? allow_smem(sparse_mla_kernel<576, 512, true>, smem, g_smem_f8)
+            : allow_smem(sparse_mla_kernel<576, 512, false>, smem, g_smem_big);
     if (st != DSA_OK) return st;
     // the two value halves of a (token, split) form a 2-CTA cluster
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = MlaSmem<576, 512>::kTotal;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -835,13 +1016,15 @@ dsa_status_t launch_mla(const MlaParams& p, const void* q, const void* kv, int D
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel<576, 512>, p, qmap, kvmap, qmap64, kvmap64);
+    cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, sparse_mla_kernel<576, 512, true>, p, qmap, kvmap, qmap64, kvmap64, scmap)
+                       : cudaLaunchKernelEx(&cfg, sparse_mla_kernel<576, 512, false>, p, qmap, kvmap, qmap64, kvmap64,
+                                            scmap);
     if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "sparse_mla_kernel launch failed: %s", cudaGetErrorString(e));
   } else {
-    st = allow_smem(sparse_mla_kernel<80, 64>, MlaSmem<80, 64>::kTotal, g_smem_tiny);
+    st = allow_smem(sparse_mla_kernel<80, 64, false>, MlaSmem<80, 64, false>::kTotal, g_smem_tiny);
     if (st != DSA_OK) return st;
-    sparse_mla_kernel<80, 64><<<static_cast<unsigned>(grid), kThreads, MlaSmem<80, 64>::kTotal, s>>>(p, qmap, kvmap, qmap64,
-                                                                                                       kvmap64);
+    sparse_mla_kernel<80, 64, false><<<static_cast<unsigned>(grid), kThreads, MlaSmem<80, 64, false>::kTotal, s>>>(
+        p, qmap, kvmap, qmap64, kvmap64, scmap);
   }
   return check_launch("sparse_mla_kernel");
 }
@@ -850,12 +1033,17 @@ dsa_status_t validate(const void* q, const void* kv_cache, int64_t kv_block_stri
                       const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
                       const int32_t* query_start_loc, const int32_t* topk_idx, int32_t B, int32_t T, int32_t H,
                       int32_t Dk, int32_t Dv, int32_t index_topk, int32_t block_size, float softmax_scale,
-                      const void* out, const char* name) {
+                      const void* out, bool f8, const char* name) {
   if (B < 0 || T < 0 || H <= 0 || index_topk <= 0 || block_size <= 0 || num_blocks < 0 || bt_stride < 0)
     return fail(DSA_ERR_INVALID_ARG, "%s: negative or zero size argument", name);
   if (T > 0 && B == 0) return fail(DSA_ERR_INVALID_ARG, "%s: T > 0 with B == 0", name);
   if (!(Dk == 576 && Dv == 512) && !(Dk == 80 && Dv == 64))
     return fail(DSA_ERR_UNSUPPORTED, "%s: (Dk, Dv) = (%d, %d) not in {(576,512), (80,64)}", name, Dk, Dv);
+  if (f8 && !(Dk == 576 && Dv == 512))
+    return fail(DSA_ERR_UNSUPPORTED, "%s: the fp8 cache supports (Dk, Dv) = (576, 512) only", name);
+  // a cache row in the units of kv_block_stride: Dk bf16 elements, or the
+  // bytes of an fp8 row
+  const int64_t row = f8 ? fp8_row_bytes(Dk, Dv) : Dk;
   if (H > 128) return fail(DSA_ERR_UNSUPPORTED, "%s: H=%d > 128", name, H);
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
     return fail(DSA_ERR_INVALID_ARG, "%s: softmax_scale must be positive and finite", name);
@@ -864,24 +1052,24 @@ dsa_status_t validate(const void* q, const void* kv_cache, int64_t kv_block_stri
     return fail(DSA_ERR_INVALID_ARG, "%s: null pointer", name);
   if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out))
     return fail(DSA_ERR_INVALID_ARG, "%s: q, kv_cache and out must be 16-byte aligned", name);
-  if (kv_block_stride < static_cast<int64_t>(block_size) * Dk)
-    return fail(DSA_ERR_INVALID_ARG, "%s: kv_block_stride %lld < block_size*Dk", name,
-                static_cast<long long>(kv_block_stride));
-  if (kv_block_stride % Dk)
-    return fail(DSA_ERR_UNSUPPORTED, "%s: kv_block_stride %lld is not a whole number of %d-element rows", name,
-                static_cast<long long>(kv_block_stride), Dk);
-  if (static_cast<int64_t>(num_blocks) * (kv_block_stride / Dk) >= (int64_t(1) << 31))
+  if (kv_block_stride < static_cast<int64_t>(block_size) * row)
+    return fail(DSA_ERR_INVALID_ARG, "%s: kv_block_stride %lld < block_size rows of %lld", name,
+                static_cast<long long>(kv_block_stride), static_cast<long long>(row));
+  if (kv_block_stride % row)
+    return fail(DSA_ERR_UNSUPPORTED, "%s: kv_block_stride %lld is not a whole number of %lld-unit rows", name,
+                static_cast<long long>(kv_block_stride), static_cast<long long>(row));
+  if (static_cast<int64_t>(num_blocks) * (kv_block_stride / row) >= (int64_t(1) << 31))
     return fail(DSA_ERR_UNSUPPORTED, "%s: the cache holds 2^31 rows or more", name);
   return check_device();
 }
 
-MlaParams make_params(int64_t kv_block_stride, int32_t Dk, int32_t num_blocks, const int32_t* block_table,
+MlaParams make_params(int64_t kv_block_stride, int64_t row_units, int32_t num_blocks, const int32_t* block_table,
                       int32_t bt_stride, const int32_t* seq_lens, const int32_t* query_start_loc,
                       const int32_t* topk_idx, int32_t B, int32_t T, int32_t H, int32_t index_topk, int32_t block_size,
                       float softmax_scale, int32_t splits, void* out, float* lse, int32_t* dev_status) {
   MlaParams p;
   p.num_blocks = num_blocks;
-  p.rows_per_block = static_cast<int32_t>(kv_block_stride / Dk);
+  p.rows_per_block = static_cast<int32_t>(kv_block_stride / row_units);
   p.total_rows = static_cast<int32_t>(static_cast<int64_t>(num_blocks) * p.rows_per_block);
   p.block_table = block_table;
   p.bt_stride = bt_stride;
@@ -947,6 +1135,63 @@ extern "C" int32_t sparse_mla_num_splits(int32_t T, int32_t H, int32_t Dv, int32
   return sparse_mla_auto_splits(T, H, Dv, index_topk);
 }
 
+namespace dsa {
+namespace {
+
+dsa_status_t decode_impl(const void* q, const void* kv_cache, int64_t kv_block_stride, int32_t num_blocks,
+                         const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                         const int32_t* query_start_loc, const int32_t* topk_idx, int32_t B, int32_t T, int32_t H,
+                         int32_t Dk, int32_t Dv, int32_t index_topk, int32_t block_size, float softmax_scale,
+                         int32_t num_kv_splits, void* out, float* lse, void* workspace, size_t ws_bytes,
+                         int32_t* dev_status, dsa_stream_t stream, bool f8, const char* name) {
+  dsa_status_t st = validate(q, kv_cache, kv_block_stride, num_blocks, block_table, bt_stride, seq_lens,
+                             query_start_loc, topk_idx, B, T, H, Dk, Dv, index_topk, block_size, softmax_scale, out, f8,
+                             name);
+  if (st != DSA_OK || T == 0) return st;
+  if (num_kv_splits < DSA_KV_SPLITS_BATCH_INVARIANT || num_kv_splits > 32)
+    return fail(DSA_ERR_INVALID_ARG, "%s: num_kv_splits %d not in [-1, 32]", name, num_kv_splits);
+  const int splits = sparse_mla_num_splits(T, H, Dv, index_topk, num_kv_splits);
+  if ((index_topk + splits - 1) / splits > kMaxSlots)
+    return fail(DSA_ERR_UNSUPPORTED, "%s: %d top-k slots per split exceed %d", name, (index_topk + splits - 1) / splits,
+                kMaxSlots);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  MlaParams p = make_params(kv_block_stride, f8 ? fp8_row_bytes(Dk, Dv) : Dk, num_blocks, block_table, bt_stride,
+                            seq_lens, query_start_loc, topk_idx, B, T, H, index_topk, block_size, softmax_scale,
+                            splits, out, lse, dev_status);
+  if (splits > 1) {
+    const size_t need = sparse_mla_workspace_size(T, H, Dv, splits);
+    if (workspace == nullptr || ws_bytes < need || !aligned16(workspace))
+      return fail(DSA_ERR_WORKSPACE, "%s: %d splits need %zu workspace bytes (16-byte aligned), got %zu", name, splits,
+                  need, ws_bytes);
+    p.o_part = static_cast<float*>(workspace);
+    p.ml_part = reinterpret_cast<float2*>(p.o_part + static_cast<int64_t>(T) * H * splits * Dv);
+  }
+  st = launch_mla(p, q, kv_cache, Dk, Dv, f8, s);
+  if (st != DSA_OK || splits == 1) return st;
+  return launch_merge(p, Dv, lse, s);
+}
+
+dsa_status_t prefill_impl(const void* q, const void* kv_cache, int64_t kv_block_stride, int32_t num_blocks,
+                          const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                          const int32_t* query_start_loc, const int32_t* topk_idx, int32_t B, int32_t T, int32_t H,
+                          int32_t Dk, int32_t Dv, int32_t index_topk, int32_t block_size, float softmax_scale,
+                          void* out, float* lse, int32_t* dev_status, dsa_stream_t stream, bool f8, const char* name) {
+  dsa_status_t st = validate(q, kv_cache, kv_block_stride, num_blocks, block_table, bt_stride, seq_lens,
+                             query_start_loc, topk_idx, B, T, H, Dk, Dv, index_topk, block_size, softmax_scale, out, f8,
+                             name);
+  if (st != DSA_OK || T == 0) return st;
+  if (index_topk > kMaxSlots)
+    return fail(DSA_ERR_UNSUPPORTED, "%s: index_topk %d > %d (use the decode entry point with splits)", name, index_topk,
+                kMaxSlots);
+  MlaParams p = make_params(kv_block_stride, f8 ? fp8_row_bytes(Dk, Dv) : Dk, num_blocks, block_table, bt_stride,
+                            seq_lens, query_start_loc, topk_idx, B, T, H, index_topk, block_size, softmax_scale, 1, out,
+                            lse, dev_status);
+  return launch_mla(p, q, kv_cache, Dk, Dv, f8, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace dsa
+
 extern "C" dsa_status_t sparse_mla_decode(const void* q, const void* kv_cache, int64_t kv_block_stride,
                                           int32_t num_blocks, const int32_t* block_table, int32_t bt_stride,
                                           const int32_t* seq_lens, const int32_t* query_start_loc,
@@ -954,30 +1199,9 @@ extern "C" dsa_status_t sparse_mla_decode(const void* q, const void* kv_cache, i
                                           int32_t Dv, int32_t index_topk, int32_t block_size, float softmax_scale,
                                           int32_t num_kv_splits, void* out, float* lse, void* workspace,
                                           size_t ws_bytes, int32_t* dev_status, dsa_stream_t stream) {
-  dsa_status_t st = validate(q, kv_cache, kv_block_stride, num_blocks, block_table, bt_stride, seq_lens,
-                             query_start_loc, topk_idx, B, T, H, Dk, Dv, index_topk, block_size, softmax_scale, out,
-                             "sparse_mla_decode");
-  if (st != DSA_OK || T == 0) return st;
-  if (num_kv_splits < DSA_KV_SPLITS_BATCH_INVARIANT || num_kv_splits > 32)
-    return fail(DSA_ERR_INVALID_ARG, "sparse_mla_decode: num_kv_splits %d not in [-1, 32]", num_kv_splits);
-  const int splits = sparse_mla_num_splits(T, H, Dv, index_topk, num_kv_splits);
-  if ((index_topk + splits - 1) / splits > kMaxSlots)
-    return fail(DSA_ERR_UNSUPPORTED, "sparse_mla_decode: %d top-k slots per split exceed %d", (index_topk + splits - 1) / splits,
-                kMaxSlots);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  MlaParams p = make_params(kv_block_stride, Dk, num_blocks, block_table, bt_stride, seq_lens, query_start_loc,
-                            topk_idx, B, T, H, index_topk, block_size, softmax_scale, splits, out, lse, dev_status);
-  if (splits > 1) {
-    const size_t need = sparse_mla_workspace_size(T, H, Dv, splits);
-    if (workspace == nullptr || ws_bytes < need || !aligned16(workspace))
-      return fail(DSA_ERR_WORKSPACE, "sparse_mla_decode: %d splits need %zu workspace bytes (16-byte aligned), got %zu",
-                  splits, need, ws_bytes);
-    p.o_part = static_cast<float*>(workspace);
-    p.ml_part = reinterpret_cast<float2*>(p.o_part + static_cast<int64_t>(T) * H * splits * Dv);
-  }
-  st = launch_mla(p, q, kv_cache, Dk, Dv, s);
-  if (st != DSA_OK || splits == 1) return st;
-  return launch_merge(p, Dv, lse, s);
+  return decode_impl(q, kv_cache, kv_block_stride, num_blocks, block_table, bt_stride, seq_lens, query_start_loc,
+                     topk_idx, B, T, H, Dk, Dv, index_topk, block_size, softmax_scale, num_kv_splits, out, lse,
+                     workspace, ws_bytes, dev_status, stream, false, "sparse_mla_decode");
 }
 
 extern "C" dsa_status_t sparse_mla_prefill(const void* q, const void* kv_cache, int64_t kv_block_stride,
@@ -986,16 +1210,32 @@ extern "C" dsa_status_t sparse_mla_prefill(const void* q, const void* kv_cache, 
                                            const int32_t* topk_idx, int32_t B, int32_t T, int32_t H, int32_t Dk,
                                            int32_t Dv, int32_t index_topk, int32_t block_size, float softmax_scale,
                                            void* out, float* lse, int32_t* dev_status, dsa_stream_t stream) {
-  dsa_status_t st = validate(q, kv_cache, kv_block_stride, num_blocks, block_table, bt_stride, seq_lens,
-                             query_start_loc, topk_idx, B, T, H, Dk, Dv, index_topk, block_size, softmax_scale, out,
-                             "sparse_mla_prefill");
-  if (st != DSA_OK || T == 0) return st;
-  if (index_topk > kMaxSlots)
-    return fail(DSA_ERR_UNSUPPORTED, "sparse_mla_prefill: index_topk %d > %d (use sparse_mla_decode with splits)",
-                index_topk, kMaxSlots);
-  MlaParams p = make_params(kv_block_stride, Dk, num_blocks, block_table, bt_stride, seq_lens, query_start_loc,
-                            topk_idx, B, T, H, index_topk, block_size, softmax_scale, 1, out, lse, dev_status);
-  return launch_mla(p, q, kv_cache, Dk, Dv, reinterpret_cast<cudaStream_t>(stream));
+  return prefill_impl(q, kv_cache, kv_block_stride, num_blocks, block_table, bt_stride, seq_lens, query_start_loc,
+                      topk_idx, B, T, H, Dk, Dv, index_topk, block_size, softmax_scale, out, lse, dev_status, stream,
+                      false, "sparse_mla_prefill");
+}
+
+extern "C" dsa_status_t sparse_mla_decode_fp8(const void* q, const uint8_t* kv_cache, int64_t kv_block_stride_bytes,
+                                              int32_t num_blocks, const int32_t* block_table, int32_t bt_stride,
+                                              const int32_t* seq_lens, const int32_t* query_start_loc,
+                                              const int32_t* topk_idx, int32_t B, int32_t T, int32_t H, int32_t Dk,
+                                              int32_t Dv, int32_t index_topk, int32_t block_size, float softmax_scale,
+                                              int32_t num_kv_splits, void* out, float* lse, void* workspace,
+                                              size_t ws_bytes, int32_t* dev_status, dsa_stream_t stream) {
+  return decode_impl(q, kv_cache, kv_block_stride_bytes, num_blocks, block_table, bt_stride, seq_lens,
+                     query_start_loc, topk_idx, B, T, H, Dk, Dv, index_topk, block_size, softmax_scale, num_kv_splits,
+                     out, lse, workspace, ws_bytes, dev_status, stream, true, "sparse_mla_decode_fp8");
+}
+
+extern "C" dsa_status_t sparse_mla_prefill_fp8(const void* q, const uint8_t* kv_cache, int64_t kv_block_stride_bytes,
+                                               int32_t num_blocks, const int32_t* block_table, int32_t bt_stride,
+                                               const int32_t* seq_lens, const int32_t* query_start_loc,
+                                               const int32_t* topk_idx, int32_t B, int32_t T, int32_t H, int32_t Dk,
+                                               int32_t Dv, int32_t index_topk, int32_t block_size, float softmax_scale,
+                                               void* out, float* lse, int32_t* dev_status, dsa_stream_t stream) {
+  return prefill_impl(q, kv_cache, kv_block_stride_bytes, num_blocks, block_table, bt_stride, seq_lens,
+                      query_start_loc, topk_idx, B, T, H, Dk, Dv, index_topk, block_size, softmax_scale, out, lse,
+                      dev_status, stream, true, "sparse_mla_prefill_fp8");
 }
 
 // ---------------------------------------------------------------------------

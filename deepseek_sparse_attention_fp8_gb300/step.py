@@ -50,7 +50,7 @@ def _dev(a, dtype, device):
 
 
 class DsaStep:
-    def __init__(self, wl, device="cuda", num_kv_splits: int = 0, prefill: bool | None = None):
+    def __init__(self, wl, device="cuda", num_kv_splits: int = 0, prefill: bool | None = None, kv_fp8: bool = False):
         self.wl = wl
         self.device = torch.device(device)
         d = self.device
@@ -61,7 +61,14 @@ class DsaStep:
             v.copy_(_host(a, dt))
         self.q_idx, self.w, self.q, self.block_table, self.seq_lens, self.qsl = views
         self.k_cache = _dev(wl.k_cache, torch.uint8, d)
-        self.kv_cache = _dev(wl.kv_cache, torch.bfloat16, d)
+        # the latent cache: bf16 rows, or (kv_fp8) the workload's fp8 rows
+        self.kv_fp8 = kv_fp8
+        if kv_fp8:
+            if wl.kv_cache_fp8 is None:
+                raise ValueError("the workload was built without kv_fp8=True")
+            self.kv_cache = _dev(wl.kv_cache_fp8, torch.uint8, d)
+        else:
+            self.kv_cache = _dev(wl.kv_cache, torch.bfloat16, d)
         self.logits = torch.empty((wl.T, wl.ld), dtype=torch.float32, device=d)
         self.topk_idx = torch.empty((wl.T, wl.index_topk), dtype=torch.int32, device=d)
         self.outputs, (self.out, self.lse) = _packed([((wl.T, wl.H, wl.Dv), torch.bfloat16),
@@ -86,13 +93,14 @@ class DsaStep:
 
     def attention(self, stream=None):
         wl = self.wl
+        prefill = api.sparse_mla_prefill_fp8 if self.kv_fp8 else api.sparse_mla_prefill
+        decode = api.sparse_mla_decode_fp8 if self.kv_fp8 else api.sparse_mla_decode
         if self.prefill:
-            api.sparse_mla_prefill(self.q, self.kv_cache, self.block_table, self.seq_lens, self.qsl, self.topk_idx,
-                                   wl.softmax_scale, wl.Dv, self.out, self.lse, self.dev_status, stream)
+            prefill(self.q, self.kv_cache, self.block_table, self.seq_lens, self.qsl, self.topk_idx, wl.softmax_scale,
+                    wl.Dv, self.out, self.lse, self.dev_status, stream)
         else:
-            api.sparse_mla_decode(self.q, self.kv_cache, self.block_table, self.seq_lens, self.qsl, self.topk_idx,
-                                  wl.softmax_scale, wl.Dv, self.out, self.lse, self.splits, self.ws_mla,
-                                  self.dev_status, stream)
+            decode(self.q, self.kv_cache, self.block_table, self.seq_lens, self.qsl, self.topk_idx, wl.softmax_scale,
+                   wl.Dv, self.out, self.lse, self.splits, self.ws_mla, self.dev_status, stream)
 
     def run(self, stream=None):
         self.indexer(stream)

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from oracle import dsa_oracle as O
-from deepseek_sparse_attention_fp8_gb300.inputs import make_workload
+from deepseek_sparse_attention_fp8_gb300.inputs import bf16_bits_to_float, make_workload
 
 from dsa_testlib import check_attention, check_logits, check_topk_sets, oracle_attention, oracle_logits
 
@@ -16,9 +16,9 @@ if torch.cuda.is_available():
     from deepseek_sparse_attention_fp8_gb300.step import DsaStep
 
 
-def _run(name, **kw):
-    wl = make_workload(name)
-    step = DsaStep(wl, **kw)
+def _run(name, kv_fp8=False, **kw):
+    wl = make_workload(name, kv_fp8=kv_fp8)
+    step = DsaStep(wl, kv_fp8=kv_fp8, **kw)
     step.logits.fill_(float("nan"))
     step.run()
     torch.cuda.synchronize()
@@ -87,3 +87,16 @@ def test_mixed_b64_mtp2():
     for t in short:
         valid = int(wl.seq_lens[t // 2]) - 2 + (t % 2) + 1
         assert np.array_equal(idx[t, :valid], np.arange(valid)) and np.all(idx[t, valid:] == -1)
+
+
+def test_decode_b32_l8192_fp8_cache():
+    """The bench's decode workload over the fp8 latent cache: sampled tokens
+    against the oracle's attention over the decoded cache."""
+    wl, step = _run("decode_b32_l8192", kv_fp8=True)
+    rows = [0, 17, 31]
+    idx = step.topk_idx.cpu().numpy()
+    q = bf16_bits_to_float(wl.q)
+    kv = O.mla_fp8_decode_cache(wl.kv_cache_fp8, wl.Dk, wl.Dv)
+    ref, ref_lse = O.sparse_mla(q, kv, wl.kv_block_stride, wl.block_table, wl.seq_lens, wl.query_start_loc, idx,
+                                wl.softmax_scale, wl.Dv, wl.block_size, rows=rows)
+    check_attention(step.out.float().cpu().numpy(), ref, np.array(rows), step.lse.cpu().numpy(), ref_lse)
