@@ -61,6 +61,29 @@ dsa_status_t allow_smem(K kernel, int bytes, FuncAttrOnce& once) {
   return DSA_OK;
 }
 
+// The arguments of an indexer-logits call (a0 + a1), shared by the entry
+// points that compute logits.
+struct IndexerCall {
+  const void* q_idx;
+  int64_t q_stride_t;
+  const float* w;
+  const uint8_t* k_cache;
+  int64_t k_block_stride_bytes;
+  int32_t num_blocks;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  int32_t B, T, Hi, Di, block_size, max_q_len;
+  int32_t* dev_status;
+};
+// Host-side checks of an indexer call (DSA_OK or the error, recorded).
+dsa_status_t indexer_validate(const IndexerCall& c, const char* name);
+// Enqueues the logits of keys [key_begin, key_begin + ld) into logits [T, ld]
+// (column j = key key_begin + j); requests are clipped to keys below key_cap.
+dsa_status_t indexer_launch(const IndexerCall& c, float* logits, int64_t ld, int64_t key_begin, int64_t key_cap,
+                            cudaStream_t stream);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 

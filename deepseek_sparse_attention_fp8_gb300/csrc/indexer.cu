@@ -107,6 +107,8 @@ struct IndexerParams {
   int32_t stages;
   float* logits;
   int64_t ld;
+  int64_t key_begin;  // key of logits column 0 (a window of the keys; a multiple of 128 and of block_size)
+  int64_t key_cap;    // requests are clipped to keys below this (ld for the whole-row call)
   int32_t* dev_status;
 };
 
@@ -146,14 +148,16 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = blockIdx.y / p.n_tb;
   const int tblk = blockIdx.y % p.n_tb;
+  // tiles are counted in logits columns; tile i holds keys key_begin + 128 i ..
   const int t_begin = blockIdx.x * p.tiles_per_cta;
   const int t_end = min(t_begin + p.tiles_per_cta, p.n_tiles);
+  const int kb = static_cast<int>(p.key_begin);
   // block ids of every key the CTA's tiles can address (warps 8 and 9), read
   // before the request's length is known; entries past it are never used
   // because every use first checks the key against seq_len
   const int* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-  const int blk0 = t_begin * kTileKeys / p.block_size;
-  const int n_blk = max(0, min((t_end * kTileKeys + p.block_size - 1) / p.block_size, p.bt_stride) - blk0);
+  const int blk0 = (kb + t_begin * kTileKeys) / p.block_size;
+  const int n_blk = max(0, min((kb + t_end * kTileKeys + p.block_size - 1) / p.block_size, p.bt_stride) - blk0);
   constexpr int kBlkPerThread = (kMaxBlocksPerCta + 63) / 64;
   int blk_v[kBlkPerThread];
   if (warp >= 8) {
@@ -170,14 +174,14 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   const int q_len = q1 - q0;
   int seq_len = __ldg(p.seq_lens + b);
   // clip the request to what the logits row and the block table can address
-  const int64_t cap = min(p.ld, static_cast<int64_t>(p.bt_stride) * p.block_size);
+  const int64_t cap = min(p.key_cap, static_cast<int64_t>(p.bt_stride) * p.block_size);
   if (seq_len < q_len || seq_len > cap) {
     if (tid == 0 && blockIdx.x == 0) report(p.dev_status, DSA_DEVERR_SEQ_LEN);
     seq_len = max(q_len, static_cast<int>(min(static_cast<int64_t>(seq_len), cap)));
   }
   const int max_valid = min(static_cast<int64_t>(seq_len - q_len + (tok0 + ntok - 1 - q0) + 1), cap);
 
-  const int t_comp_end = min(t_end, (max_valid + kTileKeys - 1) / kTileKeys);  // tiles needing an MMA
+  const int t_comp_end = min(t_end, (max_valid - kb + kTileKeys - 1) / kTileKeys);  // tiles needing an MMA
   const int n_comp = max(0, t_comp_end - t_begin);
   const int n_cols = p.hi_pad * p.tb;  // MMA N
   const int S = p.stages;
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   // completing on full_bar[i % S]; keys past seq_len are neither loaded nor counted
   auto issue_keys = [&](int i) {
     const int st = i % S;
-    const int key0 = (t_begin + i) * kTileKeys;
+    const int key0 = kb + (t_begin + i) * kTileKeys;
     uint32_t bytes = 0;
     int blk_u[2], off_u[2];
     bool bad = false;
@@ -341,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
         if (lane == 0) abort_now();
         break;
       }
-      const int key0 = (t_begin + i) * kTileKeys;
+      const int key0 = kb + (t_begin + i) * kTileKeys;
       if constexpr (DI == 128) {
         if (lane == 0) issue_keys(i);
       } else {
@@ -450,7 +454,8 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
         break;
       }
       tc_fence_after();
-      const int s = (t_begin + i) * kTileKeys + r;
+      const int col = (t_begin + i) * kTileKeys + r;  // logits column of this lane's key
+      const int s = kb + col;
       const float scale_k = ssc[st * kTileKeys + r];
       const bool bad = s < seq_len && !block_ok(s);
       __syncwarp();
@@ -470,13 +475,13 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
         if (g == 0) {
           const float acc = mine + slot[r];
           const float out = (s < s_valid[0] && !bad) ? acc * scale_k : -INFINITY;
-          if (s < p.ld) __stcs(p.logits + static_cast<int64_t>(s_tok[0]) * p.ld + s, out);
+          if (col < p.ld) __stcs(p.logits + static_cast<int64_t>(s_tok[0]) * p.ld + col, out);
         }
       } else {
         for (int j = g; j < ntok; j += 2) {  // one token: warp w alone (fewer than 64 head columns)
           const float acc = head_sum(buf, j, 0, p.hi_pad);
           const float out = (s < s_valid[j] && !bad) ? acc * scale_k : -INFINITY;
-          if (s < p.ld) __stcs(p.logits + static_cast<int64_t>(s_tok[j]) * p.ld + s, out);
+          if (col < p.ld) __stcs(p.logits + static_cast<int64_t>(s_tok[j]) * p.ld + col, out);
         }
       }
       tc_fence_before();
@@ -488,9 +493,9 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   // tiles entirely past every token's valid range: -inf only
   if (warp < 4) {
     for (int tile = t_begin + n_comp; tile < t_end; ++tile) {
-      const int s = tile * kTileKeys + tid;
-      if (s < p.ld)
-        for (int j = 0; j < ntok; ++j) __stcs(p.logits + static_cast<int64_t>(s_tok[j]) * p.ld + s, -INFINITY);
+      const int col = tile * kTileKeys + tid;
+      if (col < p.ld)
+        for (int j = 0; j < ntok; ++j) __stcs(p.logits + static_cast<int64_t>(s_tok[j]) * p.ld + col, -INFINITY);
     }
   }
 
@@ -524,55 +529,59 @@ extern "C" dsa_status_t dsa_quant_q(const void* q_idx, int64_t q_stride_t, int32
   return check_launch("quant_q_kernel");
 }
 
-extern "C" dsa_status_t dsa_indexer_logits(const void* q_idx, int64_t q_stride_t, const float* w,
-                                           const uint8_t* k_cache, int64_t k_block_stride_bytes, int32_t num_blocks,
-                                           const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
-                                           const int32_t* query_start_loc, int32_t B, int32_t T, int32_t Hi,
-                                           int32_t Di, int32_t block_size, int32_t max_q_len, float* logits,
-                                           int64_t ld, int32_t* dev_status, dsa_stream_t stream) {
-  if (B < 0 || T < 0 || Hi <= 0 || Di <= 0 || block_size <= 0 || max_q_len < 0 || ld <= 0 || num_blocks < 0 ||
-      bt_stride < 0)
-    return fail(DSA_ERR_INVALID_ARG, "dsa_indexer_logits: negative or zero size argument");
-  if (B == 0 || T == 0) return DSA_OK;
-  if (!q_idx || !w || !k_cache || !block_table || !seq_lens || !query_start_loc || !logits)
-    return fail(DSA_ERR_INVALID_ARG, "dsa_indexer_logits: null pointer");
-  if (max_q_len < 1) return fail(DSA_ERR_INVALID_ARG, "dsa_indexer_logits: max_q_len must be >= 1 when T > 0");
-  if (Hi > 64) return fail(DSA_ERR_UNSUPPORTED, "dsa_indexer_logits: Hi=%d > 64", Hi);
-  if (Di != 32 && Di != 64 && Di != 128) return fail(DSA_ERR_UNSUPPORTED, "dsa_indexer_logits: Di=%d not in {32,64,128}", Di);
-  if (block_size % 64) return fail(DSA_ERR_UNSUPPORTED, "dsa_indexer_logits: block_size %d not a multiple of 64", block_size);
-  if (k_block_stride_bytes < static_cast<int64_t>(block_size) * (Di + 4) || k_block_stride_bytes % 16)
-    return fail(DSA_ERR_INVALID_ARG, "dsa_indexer_logits: k_block_stride_bytes %lld must be >= block_size*(Di+4) and a multiple of 16",
-                static_cast<long long>(k_block_stride_bytes));
-  if (!aligned16(q_idx) || !aligned16(k_cache) || q_stride_t < static_cast<int64_t>(Hi) * Di || q_stride_t % 8)
-    return fail(DSA_ERR_INVALID_ARG, "dsa_indexer_logits: q_idx/k_cache must be 16-byte aligned, q token stride >= Hi*Di and a multiple of 8");
-  if (!aligned4(w) || !aligned4(logits)) return fail(DSA_ERR_INVALID_ARG, "dsa_indexer_logits: misaligned w/logits");
-  dsa_status_t st = check_device();
-  if (st != DSA_OK) return st;
+namespace dsa {
 
+dsa_status_t indexer_validate(const IndexerCall& c, const char* name) {
+  if (c.B < 0 || c.T < 0 || c.Hi <= 0 || c.Di <= 0 || c.block_size <= 0 || c.max_q_len < 0 || c.num_blocks < 0 ||
+      c.bt_stride < 0)
+    return fail(DSA_ERR_INVALID_ARG, "%s: negative or zero size argument", name);
+  if (c.B == 0 || c.T == 0) return DSA_OK;
+  if (!c.q_idx || !c.w || !c.k_cache || !c.block_table || !c.seq_lens || !c.query_start_loc)
+    return fail(DSA_ERR_INVALID_ARG, "%s: null pointer", name);
+  if (c.max_q_len < 1) return fail(DSA_ERR_INVALID_ARG, "%s: max_q_len must be >= 1 when T > 0", name);
+  if (c.Hi > 64) return fail(DSA_ERR_UNSUPPORTED, "%s: Hi=%d > 64", name, c.Hi);
+  if (c.Di != 32 && c.Di != 64 && c.Di != 128) return fail(DSA_ERR_UNSUPPORTED, "%s: Di=%d not in {32,64,128}", name, c.Di);
+  if (c.block_size % 64) return fail(DSA_ERR_UNSUPPORTED, "%s: block_size %d not a multiple of 64", name, c.block_size);
+  if (c.k_block_stride_bytes < static_cast<int64_t>(c.block_size) * (c.Di + 4) || c.k_block_stride_bytes % 16)
+    return fail(DSA_ERR_INVALID_ARG, "%s: k_block_stride_bytes %lld must be >= block_size*(Di+4) and a multiple of 16",
+                name, static_cast<long long>(c.k_block_stride_bytes));
+  if (!aligned16(c.q_idx) || !aligned16(c.k_cache) || c.q_stride_t < static_cast<int64_t>(c.Hi) * c.Di ||
+      c.q_stride_t % 8)
+    return fail(DSA_ERR_INVALID_ARG,
+                "%s: q_idx/k_cache must be 16-byte aligned, q token stride >= Hi*Di and a multiple of 8", name);
+  if (!aligned4(c.w)) return fail(DSA_ERR_INVALID_ARG, "%s: misaligned w", name);
+  return check_device();
+}
+
+dsa_status_t indexer_launch(const IndexerCall& c, float* logits, int64_t ld, int64_t key_begin, int64_t key_cap,
+                            cudaStream_t s) {
   IndexerParams p;
-  p.q = static_cast<const uint16_t*>(q_idx);
-  p.q_stride_t = q_stride_t;
-  p.w = w;
-  p.k_cache = k_cache;
-  p.k_block_stride = k_block_stride_bytes;
-  p.num_blocks = num_blocks;
-  p.block_table = block_table;
-  p.bt_stride = bt_stride;
-  p.seq_lens = seq_lens;
-  p.qsl = query_start_loc;
-  p.B = B;
-  p.Hi = Hi;
-  p.Di = Di;
-  p.block_size = block_size;
-  p.hi_pad = (Hi + 15) / 16 * 16;
-  p.tb = std::min(std::min(max_q_len, kMaxTokensPerCta), 256 / p.hi_pad);
-  p.n_tb = (max_q_len + p.tb - 1) / p.tb;
+  p.q = static_cast<const uint16_t*>(c.q_idx);
+  p.q_stride_t = c.q_stride_t;
+  p.w = c.w;
+  p.k_cache = c.k_cache;
+  p.k_block_stride = c.k_block_stride_bytes;
+  p.num_blocks = c.num_blocks;
+  p.block_table = c.block_table;
+  p.bt_stride = c.bt_stride;
+  p.seq_lens = c.seq_lens;
+  p.qsl = c.query_start_loc;
+  p.B = c.B;
+  p.Hi = c.Hi;
+  p.Di = c.Di;
+  p.block_size = c.block_size;
+  p.hi_pad = (c.Hi + 15) / 16 * 16;
+  p.tb = std::min(std::min(c.max_q_len, kMaxTokensPerCta), 256 / p.hi_pad);
+  p.n_tb = (c.max_q_len + p.tb - 1) / p.tb;
   p.n_tiles = static_cast<int32_t>((ld + kTileKeys - 1) / kTileKeys);
   p.logits = logits;
   p.ld = ld;
-  p.dev_status = dev_status;
-  const int64_t rows = static_cast<int64_t>(B) * p.n_tb;
-  if (rows > 65535) return fail(DSA_ERR_UNSUPPORTED, "dsa_indexer_logits: B * token blocks = %lld > 65535", (long long)rows);
+  p.key_begin = key_begin;
+  p.key_cap = key_cap;
+  p.dev_status = c.dev_status;
+  const int64_t rows = static_cast<int64_t>(c.B) * p.n_tb;
+  if (rows > 65535) return fail(DSA_ERR_UNSUPPORTED, "indexer: B * token blocks = %lld > 65535", (long long)rows);
+  if (key_begin + ld > 0x7FFFFFFF) return fail(DSA_ERR_UNSUPPORTED, "indexer: key positions beyond int32");
   // one wave of two CTAs per SM when the work allows it, at least two tiles per CTA
   const int64_t slots = 2LL * num_sms();
   const int64_t total_tiles = rows * p.n_tiles;
@@ -586,16 +595,16 @@ extern "C" dsa_status_t dsa_indexer_logits(const void* q_idx, int64_t q_stride_t
                                 std::max(indexer_smem(128, indexer_stages(128)).total, indexer_smem(256, indexer_stages(256)).total));
   CUtensorMap kmap;
   memset(&kmap, 0, sizeof(kmap));
-  if (Di == 128) {
-    const uint64_t dims[3] = {128, static_cast<uint64_t>(block_size), static_cast<uint64_t>(std::max(num_blocks, 1))};
-    const uint64_t strides[2] = {128, static_cast<uint64_t>(k_block_stride_bytes)};
+  dsa_status_t st;
+  if (c.Di == 128) {
+    const uint64_t dims[3] = {128, static_cast<uint64_t>(c.block_size), static_cast<uint64_t>(std::max(c.num_blocks, 1))};
+    const uint64_t strides[2] = {128, static_cast<uint64_t>(c.k_block_stride_bytes)};
     const uint32_t box[3] = {128, 64, 1};
-    st = make_tmap(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, k_cache, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    st = make_tmap(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c.k_cache, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != DSA_OK) return st;
   }
   dim3 grid((p.n_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta, static_cast<unsigned>(rows));
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  switch (Di) {
+  switch (c.Di) {
     case 128:
       st = allow_smem(indexer_logits_kernel<128>, max_smem, g_smem_set[0]);
       if (st != DSA_OK) return st;
@@ -613,4 +622,22 @@ extern "C" dsa_status_t dsa_indexer_logits(const void* q_idx, int64_t q_stride_t
       break;
   }
   return check_launch("indexer_logits_kernel");
+}
+
+}  // namespace dsa
+
+extern "C" dsa_status_t dsa_indexer_logits(const void* q_idx, int64_t q_stride_t, const float* w,
+                                           const uint8_t* k_cache, int64_t k_block_stride_bytes, int32_t num_blocks,
+                                           const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                           const int32_t* query_start_loc, int32_t B, int32_t T, int32_t Hi,
+                                           int32_t Di, int32_t block_size, int32_t max_q_len, float* logits,
+                                           int64_t ld, int32_t* dev_status, dsa_stream_t stream) {
+  const IndexerCall c = {q_idx, q_stride_t, w, k_cache, k_block_stride_bytes, num_blocks, block_table, bt_stride,
+                         seq_lens, query_start_loc, B, T, Hi, Di, block_size, max_q_len, dev_status};
+  if (ld <= 0) return fail(DSA_ERR_INVALID_ARG, "dsa_indexer_logits: ld must be positive");
+  dsa_status_t st = indexer_validate(c, "dsa_indexer_logits");
+  if (st != DSA_OK || B == 0 || T == 0) return st;
+  if (!logits) return fail(DSA_ERR_INVALID_ARG, "dsa_indexer_logits: null pointer");
+  if (!aligned4(logits)) return fail(DSA_ERR_INVALID_ARG, "dsa_indexer_logits: misaligned logits");
+  return indexer_launch(c, logits, ld, 0, ld, reinterpret_cast<cudaStream_t>(stream));
 }

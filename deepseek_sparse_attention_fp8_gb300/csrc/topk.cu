@@ -188,6 +188,15 @@ __device__ void find_bin(TopkShared& sh, uint32_t need) {
   __syncthreads();
 }
 
+// Output modes. kPositions: the selected positions of each row, -1 padded
+// (dsa_topk). kWindow: the row is one window of the keys, starting at key
+// key_begin; its n = min(k, valid keys in the window) selections go, with
+// their values, to the candidate arrays at the window's offset (window index
+// x kcand, kcand = min(k, win)), no padding. kFinal: the row is the
+// candidate array itself (positions = candidate slots, ascending in key);
+// the selected slots' keys are written, -1 padded.
+enum TopkMode { kPositions = 0, kWindow = 1, kFinal = 2 };
+
 struct TopkParams {
   const float* logits;
   int64_t ld;
@@ -195,10 +204,47 @@ struct TopkParams {
   const int32_t* qsl;
   int B, k, parts;
   int32_t* out;
+  int mode;
+  int64_t key_begin;
+  int32_t win, kcand, cand_stride;
+  float* cand_val;
+  int32_t* cand_idx;
 };
 
+// The row's length in the mode's own positions, from the token's valid
+// length v (keys 0..v-1) clipped to ld.
+template <int MODE>
+__device__ __forceinline__ int row_length(const TopkParams& p, int v) {
+  if constexpr (MODE == kWindow) return static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(v) - p.key_begin, p.ld)));
+  if constexpr (MODE == kFinal) {
+    const int full = v / p.win, rem = v - full * p.win;
+    return static_cast<int>(min(static_cast<int64_t>(full) * p.kcand + min(p.kcand, rem), p.ld));
+  }
+  return static_cast<int>(min(static_cast<int64_t>(v), p.ld));
+}
+
+// Writes selection `slot` (position `pos` of row t, value `val`) in the mode's form.
+template <int MODE>
+__device__ __forceinline__ void emit(const TopkParams& p, int t, int slot, int pos, float val) {
+  if constexpr (MODE == kWindow) {
+    const int64_t at = static_cast<int64_t>(t) * p.cand_stride + (p.key_begin / p.win) * p.kcand + slot;
+    p.cand_idx[at] = static_cast<int32_t>(p.key_begin + pos);
+    p.cand_val[at] = val;
+  } else if constexpr (MODE == kFinal) {
+    p.out[static_cast<int64_t>(t) * p.k + slot] = __ldg(p.cand_idx + static_cast<int64_t>(t) * p.cand_stride + pos);
+  } else {
+    (void)val;
+    p.out[static_cast<int64_t>(t) * p.k + slot] = pos;
+  }
+}
+// An empty slot (slot >= the row's length): -1, except in window mode.
+template <int MODE>
+__device__ __forceinline__ void emit_empty(const TopkParams& p, int t, int slot) {
+  if constexpr (MODE != kWindow) p.out[static_cast<int64_t>(t) * p.k + slot] = -1;
+}
+
 // kCached: the part's keys are staged in shared memory (else re-read)
-template <bool kCached>
+template <bool kCached, int MODE>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   extern __shared__ uint32_t kc[];  // this part's keys (when cached)
   __shared__ TopkShared sh;
@@ -211,10 +257,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   // valid length comes from the step's inputs, which that kernel does not
   // write, so it is found first; then wait for the logits and let the next
   // kernel's CTAs be scheduled.
-  const int n = valid_length(p.seq_lens, p.qsl, p.B, t, p.ld, sh);
+  const int n = row_length<MODE>(p, valid_length(p.seq_lens, p.qsl, p.B, t, 0x7FFFFFFF, sh));
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  int32_t* out = p.out + static_cast<int64_t>(t) * k;
   const float* row = p.logits + static_cast<int64_t>(t) * p.ld;
   // The row's parts are cut by ld, so the first values are loaded whatever
   // valid(t) is; positions at or past valid(t) are ignored afterwards.
@@ -236,7 +281,10 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   if (n <= k) {  // every valid position, then -1 (the same branch for the whole cluster)
     const int o0 = static_cast<int>(static_cast<int64_t>(r) * k / P);
     const int o1 = static_cast<int>(static_cast<int64_t>(r + 1) * k / P);
-    for (int i = o0 + tid; i < o1; i += kThreads) out[i] = i < n ? i : -1;
+    for (int i = o0 + tid; i < o1; i += kThreads) {
+      if (i < n) emit<MODE>(p, t, i, i, MODE == kWindow ? __ldg(row + i) : 0.f);
+      else emit_empty<MODE>(p, t, i);
+    }
     return;
   }
   // Rows that keep a small fraction of their keys record, per warp and in
@@ -535,8 +583,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     const bool gt = c < c1 && key > thr, eq = c < c1 && key == thr;
     const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), be = __ballot_sync(0xFFFFFFFFu, eq);
     const uint32_t gi = g + __popc(bg & lt), ei = e + __popc(be & lt);
-    if (gt) out[gi + min(ei, nq)] = s0 + i;
-    if (eq && ei < nq) out[gi + ei] = s0 + i;
+    if (gt) emit<MODE>(p, t, static_cast<int>(gi + min(ei, nq)), s0 + i, key_value(key));
+    if (eq && ei < nq) emit<MODE>(p, t, static_cast<int>(gi + ei), s0 + i, key_value(key));
     g += __popc(bg);
     e += __popc(be);
   }
@@ -548,7 +596,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
 // compaction needs only ballots within a warp and one scan over the warps.
 // The bins span the row's exact finite range; the steps are those of
 // topk_kernel with P = 1.
-template <int VPT>
+template <int VPT, int MODE>
 __global__ void __launch_bounds__(kThreads) topk_row_kernel(const TopkParams p) {
   __shared__ TopkShared sh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -556,15 +604,17 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const TopkParams p) 
   const int k = p.k;
   // the row's valid length comes from the step's inputs, which the logits
   // producer does not write: it is found while that kernel may still run
-  const int n = valid_length(p.seq_lens, p.qsl, p.B, t, p.ld, sh);
+  const int n = row_length<MODE>(p, valid_length(p.seq_lens, p.qsl, p.B, t, 0x7FFFFFFF, sh));
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  int32_t* out = p.out + static_cast<int64_t>(t) * k;
+  const float* row = p.logits + static_cast<int64_t>(t) * p.ld;
   if (n <= k) {
-    for (int i = tid; i < k; i += kThreads) out[i] = i < n ? i : -1;
+    for (int i = tid; i < k; i += kThreads) {
+      if (i < n) emit<MODE>(p, t, i, i, MODE == kWindow ? __ldg(row + i) : 0.f);
+      else emit_empty<MODE>(p, t, i);
+    }
     return;
   }
-  const float* row = p.logits + static_cast<int64_t>(t) * p.ld;
   const int ld = static_cast<int>(p.ld);
   const int base = warp * 32 * VPT + lane;  // position of key[0]; key[u] sits at base + 32 u
   uint32_t key[VPT];
@@ -700,14 +750,14 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const TopkParams p) 
     const bool gt = valid(u) && key[u] > thr, eq = valid(u) && key[u] == thr;
     const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), be = __ballot_sync(0xFFFFFFFFu, eq);
     const uint32_t gi = g + __popc(bg & lt), ei = e + __popc(be & lt);
-    if (gt) out[gi + min(ei, nq)] = base + 32 * u;
-    if (eq && ei < nq) out[gi + ei] = base + 32 * u;
+    if (gt) emit<MODE>(p, t, static_cast<int>(gi + min(ei, nq)), base + 32 * u, key_value(key[u]));
+    if (eq && ei < nq) emit<MODE>(p, t, static_cast<int>(gi + ei), base + 32 * u, key_value(key[u]));
     g += __popc(bg);
     e += __popc(be);
   }
 }
 
-FuncAttrOnce g_smem, g_smem_u;
+FuncAttrOnce g_smem[3], g_smem_u[3];  // per output mode
 
 // CTAs per row: more only for long rows (at least 8192 keys per CTA) while
 // they fill the GPU once (at most 8), and enough that a part fits the
@@ -718,6 +768,63 @@ int parts_for(int32_t T, int64_t ld) {
   while (P < kMaxParts && static_cast<int64_t>(T) * P * 2 <= num_sms() && (ld + 2 * P - 1) / (2 * P) >= 8192) P *= 2;
   while (P < kMaxParts && (ld + P - 1) / P > kSegCap) P *= 2;
   return P;
+}
+
+// Launches the top-k of rows 0..T-1 described by p in output mode MODE.
+template <int MODE>
+dsa_status_t topk_launch_mode(TopkParams p, int32_t T, cudaStream_t stream) {
+  dsa_status_t st;
+  const int64_t ld = p.ld;
+  p.parts = parts_for(T, ld);
+  if (p.parts == 1 && ld <= 32 * 32 * 32) {  // one CTA per row, the row in registers
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(T));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = ld <= 32 * 8 * 32 ? cudaLaunchKernelEx(&cfg, topk_row_kernel<8, MODE>, p)
+                                            : cudaLaunchKernelEx(&cfg, topk_row_kernel<32, MODE>, p);
+    if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "topk_row_kernel launch failed: %s", cudaGetErrorString(e));
+    return DSA_OK;
+  }
+  const int64_t seg = (ld + p.parts - 1) / p.parts;
+  const bool cached = seg <= kSegCap;
+  // the part's keys, then one candidate list per warp (16-bit positions)
+  constexpr int kListBytes = kWarps * kListCap * 2;
+  const int smem = cached ? static_cast<int>(((seg + 7) & ~7) * 4) + kListBytes : 0;
+  st = cached ? allow_smem(topk_kernel<true, MODE>, kSegCap * 4 + kListBytes, g_smem[MODE])
+              : allow_smem(topk_kernel<false, MODE>, 0, g_smem_u[MODE]);
+  if (st != DSA_OK) return st;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(T) * p.parts));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.parts;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cached ? cudaLaunchKernelEx(&cfg, topk_kernel<true, MODE>, p)
+                         : cudaLaunchKernelEx(&cfg, topk_kernel<false, MODE>, p);
+  if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "topk_kernel launch failed: %s", cudaGetErrorString(e));
+  return DSA_OK;
+}
+
+dsa_status_t topk_launch(const TopkParams& p, int32_t T, cudaStream_t stream) {
+  switch (p.mode) {
+    case kWindow: return topk_launch_mode<kWindow>(p, T, stream);
+    case kFinal: return topk_launch_mode<kFinal>(p, T, stream);
+    default: return topk_launch_mode<kPositions>(p, T, stream);
+  }
 }
 
 }  // namespace
@@ -747,7 +854,7 @@ extern "C" dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t*
   if (static_cast<int64_t>(T) * kMaxParts > 0x7FFFFFFF) return fail(DSA_ERR_UNSUPPORTED, "dsa_topk: T too large");
   dsa_status_t st = check_device();
   if (st != DSA_OK) return st;
-  TopkParams p;
+  TopkParams p = {};
   p.logits = logits;
   p.ld = ld;
   p.seq_lens = seq_lens;
@@ -755,45 +862,110 @@ extern "C" dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t*
   p.B = B;
   p.k = index_topk;
   p.out = topk_idx;
-  p.parts = parts_for(T, ld);
-  if (p.parts == 1 && ld <= 32 * 32 * 32) {  // one CTA per row, the row in registers
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(T));
-    cfg.blockDim = dim3(kThreads);
-    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = ld <= 32 * 8 * 32 ? cudaLaunchKernelEx(&cfg, topk_row_kernel<8>, p)
-                                            : cudaLaunchKernelEx(&cfg, topk_row_kernel<32>, p);
-    if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "topk_row_kernel launch failed: %s", cudaGetErrorString(e));
-    return DSA_OK;
-  }
-  const int64_t seg = (ld + p.parts - 1) / p.parts;
-  const bool cached = seg <= kSegCap;
-  // the part's keys, then one candidate list per warp (16-bit positions)
-  constexpr int kListBytes = kWarps * kListCap * 2;
-  const int smem = cached ? static_cast<int>(((seg + 7) & ~7) * 4) + kListBytes : 0;
-  st = cached ? allow_smem(topk_kernel<true>, kSegCap * 4 + kListBytes, g_smem)
-              : allow_smem(topk_kernel<false>, 0, g_smem_u);
+  p.mode = kPositions;
+  return topk_launch(p, T, reinterpret_cast<cudaStream_t>(stream));
+}
+
+
+// ---------------------------------------------------------------------------
+// a1 + a2 over key windows (vLLM PR #38476 review thread: the decode logits
+// buffer is [batch, max_seq_len] fp32; windowing the keys, a top-k per window
+// giving (score, global id) candidates and one final top-k over the
+// concatenated candidates bound it, and recover the global top-k exactly,
+// since any key of the global top-k is in its window's top-k).
+namespace dsa {
+namespace {
+
+struct WindowPlan {
+  int64_t W, n_win, kcand, stride;  // window, windows, candidates per window, candidate row stride
+  size_t logits_bytes, cand_bytes, total;
+};
+
+WindowPlan window_plan(int32_t T, int64_t max_seq_len, int32_t window, int32_t index_topk) {
+  WindowPlan w = {};
+  w.W = window > 0 ? window : (max_seq_len + 127) / 128 * 128;
+  w.n_win = (max_seq_len + w.W - 1) / w.W;
+  w.kcand = std::min<int64_t>(index_topk, w.W);
+  w.stride = (w.n_win * w.kcand + 3) / 4 * 4;
+  auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+  w.logits_bytes = up(static_cast<size_t>(T) * w.W * 4);
+  w.cand_bytes = up(static_cast<size_t>(T) * w.stride * 4);
+  w.total = w.logits_bytes + (w.n_win > 1 ? 2 * w.cand_bytes : 0);
+  return w;
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" size_t dsa_indexer_topk_workspace_size(int32_t T, int64_t max_seq_len, int32_t window,
+                                                  int32_t index_topk) {
+  if (T <= 0 || max_seq_len <= 0 || index_topk <= 0 || window < 0) return 0;
+  return window_plan(T, max_seq_len, window, index_topk).total;
+}
+
+extern "C" dsa_status_t dsa_indexer_topk(const void* q_idx, int64_t q_stride_t, const float* w,
+                                         const uint8_t* k_cache, int64_t k_block_stride_bytes, int32_t num_blocks,
+                                         const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                         const int32_t* query_start_loc, int32_t B, int32_t T, int32_t Hi, int32_t Di,
+                                         int32_t block_size, int32_t max_q_len, int64_t max_seq_len, int32_t window,
+                                         int32_t index_topk, int32_t* topk_idx, void* workspace, size_t ws_bytes,
+                                         int32_t* dev_status, dsa_stream_t stream) {
+  const IndexerCall c = {q_idx, q_stride_t, w, k_cache, k_block_stride_bytes, num_blocks, block_table, bt_stride,
+                         seq_lens, query_start_loc, B, T, Hi, Di, block_size, max_q_len, dev_status};
+  dsa_status_t st = indexer_validate(c, "dsa_indexer_topk");
   if (st != DSA_OK) return st;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(T) * p.parts));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.parts;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  cudaError_t e = cached ? cudaLaunchKernelEx(&cfg, topk_kernel<true>, p) : cudaLaunchKernelEx(&cfg, topk_kernel<false>, p);
-  if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "topk_kernel launch failed: %s", cudaGetErrorString(e));
-  return DSA_OK;
+  if (max_seq_len <= 0 || index_topk <= 0 || window < 0)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_indexer_topk: max_seq_len, index_topk must be positive and window >= 0");
+  if (B == 0 || T == 0) return DSA_OK;
+  if (!topk_idx) return fail(DSA_ERR_INVALID_ARG, "dsa_indexer_topk: null pointer");
+  if (window % 128 || window % block_size)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_indexer_topk: window %d must be a multiple of 128 and of block_size", window);
+  if (index_topk > 65535) return fail(DSA_ERR_UNSUPPORTED, "dsa_indexer_topk: index_topk %d > 65535", index_topk);
+  const WindowPlan pl = window_plan(T, max_seq_len, window, index_topk);
+  if (pl.n_win * pl.W > 0x7FFFFFFF || pl.stride > 0x7FFFFFFF)
+    return fail(DSA_ERR_UNSUPPORTED, "dsa_indexer_topk: positions beyond int32");
+  if (workspace == nullptr || ws_bytes < pl.total || !aligned16(workspace))
+    return fail(DSA_ERR_WORKSPACE, "dsa_indexer_topk: %zu workspace bytes needed (16-byte aligned), got %zu", pl.total,
+                ws_bytes);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* logits = static_cast<float*>(workspace);
+  const int64_t key_cap = pl.n_win * pl.W;
+  TopkParams p = {};
+  p.seq_lens = seq_lens;
+  p.qsl = query_start_loc;
+  p.B = B;
+  p.k = index_topk;
+  p.out = topk_idx;
+  if (pl.n_win == 1) {  // one window: the plain logits + top-k on the workspace row
+    st = indexer_launch(c, logits, pl.W, 0, key_cap, s);
+    if (st != DSA_OK) return st;
+    p.logits = logits;
+    p.ld = pl.W;
+    p.mode = kPositions;
+    return topk_launch(p, T, s);
+  }
+  float* cand_val = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.logits_bytes);
+  int32_t* cand_idx = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + pl.logits_bytes + pl.cand_bytes);
+  p.win = static_cast<int32_t>(pl.W);
+  p.kcand = static_cast<int32_t>(pl.kcand);
+  p.cand_stride = static_cast<int32_t>(pl.stride);
+  p.cand_val = cand_val;
+  p.cand_idx = cand_idx;
+  for (int64_t wi = 0; wi < pl.n_win; ++wi) {
+    // the window's logits reuse one buffer: the logits kernel is not a
+    // programmatic dependent, so it starts after the previous window's top-k
+    st = indexer_launch(c, logits, pl.W, wi * pl.W, key_cap, s);
+    if (st != DSA_OK) return st;
+    p.logits = logits;
+    p.ld = pl.W;
+    p.mode = kWindow;
+    p.key_begin = wi * pl.W;
+    st = topk_launch(p, T, s);
+    if (st != DSA_OK) return st;
+  }
+  p.logits = cand_val;
+  p.ld = pl.stride;
+  p.mode = kFinal;
+  p.key_begin = 0;
+  return topk_launch(p, T, s);
 }

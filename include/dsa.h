@@ -36,6 +36,11 @@
  *     OR-ed into *dev_status when dev_status is non-NULL.
  *   - Every wait inside a kernel is bounded (about one second); a wait that
  *     runs out sets DSA_DEVERR_TIMEOUT and the kernel returns.
+ *   - The top-k, attention and merge kernels are launched as programmatic
+ *     dependents of the kernel before them on the stream. Before waiting for
+ *     it they read only inputs that no kernel of this library writes (q,
+ *     seq_lens, query_start_loc); a caller's kernel placed directly before
+ *     them that lets its dependents start early must not write those.
  *   - Request b owns query tokens [query_start_loc[b], query_start_loc[b+1]);
  *     q_len_b is their count. seq_lens[b] counts the request's cached keys
  *     INCLUDING its q_len_b new tokens, so query token t of request b sits at
@@ -54,6 +59,15 @@
  *   Latent KV cache (bf16): block p starts at element p * kv_block_stride;
  *   inside it block_size rows of Dk bf16 (Dk = 576: 512 latent + 64 rope).
  *   The value vector of a row is its first Dv elements.
+ *   Latent KV cache (fp8, Dk = 576, Dv = 512): block p starts at byte
+ *   p * kv_block_stride_bytes (a whole number, >= block_size, of 656-byte
+ *   rows); inside it block_size rows of 656 bytes: 512 e4m3 codes of the
+ *   latent dims, then 4 fp32 scales (one per 128-dim group, little-endian),
+ *   then the 64 rope dims as bf16. A latent value is e4m3(code) * scale of
+ *   its group; a group is quantised with scale = amax/448 (1 when amax == 0)
+ *   and code = e4m3_rn_satfinite(x / scale). vLLM PR #38476 (Limitations,
+ *   review thread) names FP8-KV sparse-MLA backends for SM90+/SM12x parts but
+ *   prints no layout; this is the layout this library reads and writes.
  */
 #ifndef DSA_H_
 #define DSA_H_
@@ -165,6 +179,36 @@ dsa_status_t dsa_topk(const float* logits, int64_t ld, const int32_t* seq_lens, 
                       dsa_stream_t stream);
 
 /*
+ * a1 + a2 with a bounded logits buffer: the indexer logits and the top-k
+ * computed over windows of `window` keys (vLLM PR #38476 review thread: the
+ * [batch, max_seq_len] fp32 decode logits buffer is bounded by windowing the
+ * keys, taking a top-k per window as (score, key) candidates and one final
+ * top-k over the concatenated candidates; any key of the global top-k is in
+ * its window's top-k, so the result is exact).
+ * Arguments as dsa_indexer_logits, then:
+ *   max_seq_len  upper bound of seq_lens (a longer request is clipped to the
+ *                windows covering it and sets DSA_DEVERR_SEQ_LEN)
+ *   window       keys per window, a multiple of 128 and of block_size; 0 =
+ *                one window of max_seq_len (rounded up to 128)
+ *   topk_idx     int32 [T, index_topk], exactly dsa_topk's result on the
+ *                logits of dsa_indexer_logits (the same selection, ascending
+ *                key positions, -1 padded)
+ *   workspace    dsa_indexer_topk_workspace_size(T, max_seq_len, window,
+ *                index_topk) bytes, 16-byte aligned: a [T, window] fp32 logits
+ *                buffer and, with several windows, the candidates (value and
+ *                key, [T, windows * min(index_topk, window)] each).
+ * Kernels per call: a logits kernel and a top-k kernel per window, and one
+ * final top-k when there are several windows.
+ */
+size_t dsa_indexer_topk_workspace_size(int32_t T, int64_t max_seq_len, int32_t window, int32_t index_topk);
+dsa_status_t dsa_indexer_topk(const void* q_idx, int64_t q_stride_t, const float* w, const uint8_t* k_cache,
+                              int64_t k_block_stride_bytes, int32_t num_blocks, const int32_t* block_table,
+                              int32_t bt_stride, const int32_t* seq_lens, const int32_t* query_start_loc, int32_t B,
+                              int32_t T, int32_t Hi, int32_t Di, int32_t block_size, int32_t max_q_len,
+                              int64_t max_seq_len, int32_t window, int32_t index_topk, int32_t* topk_idx,
+                              void* workspace, size_t ws_bytes, int32_t* dev_status, dsa_stream_t stream);
+
+/*
  * a3 (+ a4): sparse MLA decode with split-KV.
  *   q         bf16 [T, H, Dk] (contiguous)
  *   kv_cache  bf16 paged latent cache (layout above)
@@ -224,6 +268,53 @@ dsa_status_t sparse_mla_prefill(const void* q, const void* kv_cache, int64_t kv_
                                 int32_t H, int32_t Dk, int32_t Dv, int32_t index_topk, int32_t block_size,
                                 float softmax_scale, void* out, float* lse, int32_t* dev_status,
                                 dsa_stream_t stream);
+
+/*
+ * a3 (+ a4) over the fp8 latent cache (layout above): the same calls,
+ * arguments and results as sparse_mla_decode / sparse_mla_prefill, with
+ * kv_cache the fp8 cache and its block stride in bytes. Each CTA gathers the
+ * 256 code bytes of its half of the latent dims, the row's 16 scale bytes and
+ * its 32 rope dims (336 of the row's 656 bytes; 576 of 1152 for bf16) and
+ * dequantises the codes to bf16 (code * scale, rounded to nearest even) in
+ * shared memory before the bf16 tensor-core products. Supported: (Dk, Dv) =
+ * (576, 512), H <= 128. (vLLM PR #38476 Limitations and review thread: FP8
+ * latent caches on SM90+ parts.)
+ */
+dsa_status_t sparse_mla_decode_fp8(const void* q, const uint8_t* kv_cache, int64_t kv_block_stride_bytes,
+                                   int32_t num_blocks, const int32_t* block_table, int32_t bt_stride,
+                                   const int32_t* seq_lens, const int32_t* query_start_loc, const int32_t* topk_idx,
+                                   int32_t B, int32_t T, int32_t H, int32_t Dk, int32_t Dv, int32_t index_topk,
+                                   int32_t block_size, float softmax_scale, int32_t num_kv_splits, void* out,
+                                   float* lse, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                   dsa_stream_t stream);
+dsa_status_t sparse_mla_prefill_fp8(const void* q, const uint8_t* kv_cache, int64_t kv_block_stride_bytes,
+                                    int32_t num_blocks, const int32_t* block_table, int32_t bt_stride,
+                                    const int32_t* seq_lens, const int32_t* query_start_loc, const int32_t* topk_idx,
+                                    int32_t B, int32_t T, int32_t H, int32_t Dk, int32_t Dv, int32_t index_topk,
+                                    int32_t block_size, float softmax_scale, void* out, float* lse,
+                                    int32_t* dev_status, dsa_stream_t stream);
+
+/*
+ * Producer side of the fp8 latent cache: quantise the latent rows of the T
+ * new query tokens and store them in the fp8 cache (layout above), the way
+ * dsa_indexer_k_quant_and_cache stores indexer keys.
+ *   kv       bf16 [T, Dk], token stride kv_stride_t elements (>= Dk, a
+ *            multiple of 8; 16-byte aligned), one row per query token
+ *   kv_cache the fp8 latent cache, written in place: token t of request b
+ *            goes to row pos(t) % block_size of block
+ *            block_table[b, pos(t) / block_size]; nothing else is touched.
+ * Per token: four 128-dim groups of the 512 latent dims, each with scale =
+ * amax/448 (1 when amax == 0) and code = e4m3_rn_satfinite(x / scale), both
+ * divisions IEEE-rounded fp32; the 64 rope dims keep their bf16 bits. A
+ * position outside the block table (DSA_DEVERR_SEQ_LEN) or a block id outside
+ * [0, num_blocks) (DSA_DEVERR_BLOCK_OOB) skips that token. Supported: (Dk, Dv)
+ * = (576, 512), block_size a multiple of 64.
+ */
+dsa_status_t dsa_mla_kv_fp8_quant_and_cache(const void* kv, int64_t kv_stride_t, int32_t T, int32_t Dk, int32_t Dv,
+                                            uint8_t* kv_cache, int64_t kv_block_stride_bytes, int32_t num_blocks,
+                                            const int32_t* block_table, int32_t bt_stride, const int32_t* seq_lens,
+                                            const int32_t* query_start_loc, int32_t B, int32_t block_size,
+                                            int32_t* dev_status, dsa_stream_t stream);
 
 /*
  * Split-KV sparse MLA decode that allocates nothing. It serves callers that
