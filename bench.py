@@ -63,9 +63,10 @@ def dist_info():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
-def algorithmic_bytes(wl, topk_idx_host=None):
+def algorithmic_bytes(wl, topk_idx_host=None, kv_row_bytes=None):
     """Bytes each kernel must move at minimum: its inputs read once, its outputs
-    written once (gathered rows counted once per selected valid slot)."""
+    written once (gathered rows counted once per selected valid slot; a latent
+    row is Dk bf16 values, or kv_row_bytes for the fp8 cache)."""
     T, ld, K = wl.T, wl.ld, wl.index_topk
     qsl = wl.query_start_loc
     valid = []
@@ -78,7 +79,8 @@ def algorithmic_bytes(wl, topk_idx_host=None):
     indexer = key_bytes + T * wl.Hi * wl.Di * 2 + T * wl.Hi * 4 + T * ld * 4
     topk = int(np.sum(valid)) * 4 + T * K * 4
     live = np.minimum(valid, K) if topk_idx_host is None else np.sum(topk_idx_host >= 0, axis=1)
-    attention = int(np.sum(live)) * wl.Dk * 2 + T * wl.H * wl.Dk * 2 + T * wl.H * wl.Dv * 2 + T * K * 4 + T * wl.H * 4
+    row = wl.Dk * 2 if kv_row_bytes is None else kv_row_bytes
+    attention = int(np.sum(live)) * row + T * wl.H * wl.Dk * 2 + T * wl.H * wl.Dv * 2 + T * K * 4 + T * wl.H * 4
     flops_att = int(np.sum(live)) * wl.H * (2 * wl.Dk + 2 * wl.Dv)
     flops_idx = int(np.sum(valid)) * wl.Hi * wl.Di * 2
     return dict(indexer=indexer, topk=topk, attention=attention, flops_attention=flops_att, flops_indexer=flops_idx)
@@ -145,23 +147,13 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_oracle_step(wl, rows, kv_float=None, q_float=None):
-    """The oracle's DSA step for the given query rows; returns seconds."""
-    from oracle import dsa_oracle as O
-    from deepseek_sparse_attention_fp8_gb300.inputs import bf16_bits_to_float
+def cpu_oracle_step(wl, rows, threads=0):
+    """The plain C++ oracle's DSA step (a0-a3) for the given query rows on
+    `threads` host threads (0 = all hardware threads); returns seconds."""
+    from oracle import ref as R
 
-    q_float = bf16_bits_to_float(wl.q) if q_float is None else q_float
-    kv_float = bf16_bits_to_float(wl.kv_cache) if kv_float is None else kv_float
     t0 = time.perf_counter()
-    codes, scales = O.quantize_groups(bf16_bits_to_float(wl.q_idx[rows]))
-    full_codes = np.zeros(wl.q_idx.shape, np.uint8)
-    full_scales = np.ones(wl.q_idx.shape[:2], np.float32)
-    full_codes[rows], full_scales[rows] = codes, scales
-    logits = O.indexer_logits(full_codes, full_scales, wl.w, wl.k_cache, wl.k_block_stride, wl.block_table,
-                              wl.seq_lens, wl.query_start_loc, wl.block_size, wl.ld, rows=rows)
-    idx = O.topk(logits, wl.seq_lens, wl.query_start_loc, wl.index_topk, rows=rows)
-    O.sparse_mla(q_float, kv_float, wl.kv_block_stride, wl.block_table, wl.seq_lens, wl.query_start_loc, idx,
-                 wl.softmax_scale, wl.Dv, wl.block_size, rows=rows)
+    R.step(wl, rows, threads=threads)
     return time.perf_counter() - t0
 
 
@@ -191,58 +183,45 @@ def oracle_rows(T: int, n: int):
 
 
 def oracle_timed(wl, budget_s: float = 10.0):
-    """The oracle on a bounded sample of the workload's query tokens (about
-    budget_s of work): (rows, wall seconds, average busy threads = CPU time / wall)."""
-    per_tok = cpu_oracle_step(wl, [0])
-    rows = oracle_rows(wl.T, int(budget_s / max(per_tok, 1e-6)))
-    c0 = time.process_time()
-    sec = cpu_oracle_step(wl, rows)
-    return rows, sec, (time.process_time() - c0) / max(sec, 1e-9)
+    """The C++ oracle on a bounded sample of the workload's query tokens, about
+    budget_s seconds on every hardware thread: (rows, seconds, threads,
+    seconds of one token on one thread)."""
+    from oracle import ref as R
 
-
-def oracle_one_thread_seconds(workload: str, n: int):
-    """The same sample in a child process whose BLAS and OpenMP pools hold one thread."""
-    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    try:
-        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--workload", workload, "--oracle-seconds",
-                            str(n)], env=env, capture_output=True, text=True, timeout=600)
-        return float(r.stdout.strip().splitlines()[-1])
-    except (subprocess.SubprocessError, ValueError, IndexError):
-        return None
-
-
-def blas_threads():
-    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
-        if os.environ.get(var):
-            return int(os.environ[var])
-    return os.cpu_count() or 1
+    threads = R.hardware_threads()
+    one = cpu_oracle_step(wl, [0], threads=1)
+    n = int(max(1, min(wl.T, budget_s * threads / max(one, 1e-6))))
+    rows = oracle_rows(wl.T, n)
+    sec = cpu_oracle_step(wl, rows, threads=threads)
+    return rows, sec, threads, one
 
 
 def run_reference(args, wl):
-    """The oracle timed on the host cores: each step is a bounded sample of
+    """The C++ oracle timed on the host cores: each step is a bounded sample of
     query tokens of the workload (sized so the whole run stays within a few
     minutes), scaled to tokens/s."""
-    from deepseek_sparse_attention_fp8_gb300.inputs import bf16_bits_to_float
+    from oracle import ref as R
 
-    q_float = bf16_bits_to_float(wl.q)
-    kv_float = bf16_bits_to_float(wl.kv_cache)
-    per_tok = cpu_oracle_step(wl, [0], kv_float, q_float)
+    threads = R.hardware_threads()
+    one = cpu_oracle_step(wl, [0], threads=1)
     budget = 150.0 / max(1, args.steps + args.warmup)
-    n = int(max(1, min(wl.T, budget // max(per_tok, 1e-6))))
-    rows = list(range(n))
+    n = int(max(1, min(wl.T, budget * threads / max(one, 1e-6))))
+    rows = oracle_rows(wl.T, n)
     for _ in range(args.warmup):
-        cpu_oracle_step(wl, rows, kv_float, q_float)
-    times = [cpu_oracle_step(wl, rows, kv_float, q_float) for _ in range(args.steps)]
-    sec = float(np.mean(times))
-    value = n / sec
+        cpu_oracle_step(wl, rows, threads=threads)
+    times = [cpu_oracle_step(wl, rows, threads=threads) for _ in range(args.steps)]
+    sec = float(np.median(times))
+    value = len(rows) / sec
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3 * wl.T / n, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3 * wl.T / len(rows),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "context": int(wl.seq_lens.max()),
-                       "index_topk": wl.index_topk, "H": wl.H},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-                             "sample": f"{n} of {wl.T} query tokens per step (full indexer row, top-k, "
-                                       f"128-head attention), numpy float64"},
+                       "index_topk": wl.index_topk, "Hi": wl.Hi, "Di": wl.Di, "H": wl.H, "Dk": wl.Dk, "Dv": wl.Dv,
+                       "block_size": wl.block_size},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{len(rows)} of {wl.T} query tokens per step, evenly spaced (full indexer "
+                                       f"row, top-k, attention), plain C++17 oracle, {threads} std::threads",
+                             "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -311,7 +290,7 @@ def main():
 
     if args.oracle_seconds:
         wl = make_workload(args.workload)
-        print(cpu_oracle_step(wl, oracle_rows(wl.T, args.oracle_seconds)), flush=True)
+        print(cpu_oracle_step(wl, oracle_rows(wl.T, args.oracle_seconds), threads=1), flush=True)
         return
     if args.impl == "reference":
         if rank != 0:
@@ -521,25 +500,25 @@ def main():
     # steps, phases alone), on rank 0 at N=1 only
     if world == 1 and not args.no_other_workloads:
         others = {}
-        for name, splits_list in OTHER_WORKLOADS:
-            if name == wl.name:
+        for name, splits_list, fp8 in OTHER_WORKLOADS:
+            if name == wl.name and not fp8:
                 continue
-            owl = make_workload(name)
+            owl = make_workload(name, kv_fp8=fp8)
             for sp in splits_list:
-                ost = DsaStep(owl, device=step_device(local), num_kv_splits=sp)
+                ost = DsaStep(owl, device=step_device(local), num_kv_splits=sp, kv_fp8=fp8)
                 warm(ost, 3)
                 n = max(5, min(K, 30))
                 ts = summary(time_steps(ost, n))
                 oph, osum = phases_consistent(ost, ts["ms"], max(5, min(n, 10)))
-                oalg = algorithmic_bytes(owl, ost.topk_idx.cpu().numpy())
+                oalg = algorithmic_bytes(owl, ost.topk_idx.cpu().numpy(), owl.kv_row_bytes_fp8 if fp8 else None)
                 okern = kernel_table(owl, oph, oalg, peaks_doc)
                 odom = max(okern, key=lambda k_: okern[k_]["ms"])
                 obytes = oalg["indexer"] + oalg["topk"] + oalg["attention"]
-                key = name if len(splits_list) == 1 else f"{name}_splits{sp}"
+                key = (name if len(splits_list) == 1 else f"{name}_splits{sp}") + ("_fp8kv" if fp8 else "")
                 others[key] = {
                     "config": {"workload": name, "B": owl.B, "T": owl.T, "context": int(owl.seq_lens.max()),
                                "index_topk": owl.index_topk, "num_kv_splits": ost.splits,
-                               "prefill": bool(ost.prefill)},
+                               "prefill": bool(ost.prefill), "kv_cache": "fp8 (656 B/row)" if fp8 else "bf16"},
                     "value": owl.T / (ts["ms"] / 1e3), "unit": "tokens/s", "steps": n, **ts,
                     "step_GBps": obytes / (ts["ms"] / 1e3) / 1e9,
                     "step_frac": obytes / (ts["ms"] / 1e3) / 1e9 / peak,
@@ -551,13 +530,12 @@ def main():
         line["workloads"] = others
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rows, sec, busy = oracle_timed(wl)
-        sec1 = oracle_one_thread_seconds(wl.name, len(rows))
-        line["cpu_baseline"] = {"value": len(rows) / sec, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+        rows, sec, threads, one = oracle_timed(wl)
+        line["cpu_baseline"] = {"value": len(rows) / sec, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                                 "sample": f"{len(rows)} of {wl.T} query tokens, evenly spaced (full indexer row, "
-                                          f"top-k, attention), numpy float64 oracle, {sec:.1f} s",
-                                "busy_threads": round(busy, 2), "cpu_model": cpu_model(),
-                                "one_thread_value": (len(rows) / sec1) if sec1 else None}
+                                          f"top-k, attention), plain C++17 oracle on {threads} std::threads, "
+                                          f"{sec:.1f} s",
+                                "cpu_model": cpu_model(), "one_thread_value": 1.0 / one}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -568,13 +546,16 @@ def step_device(local):
     return f"cuda:{local}"
 
 
-# Workloads measured beside the headline one: (name, split counts); the
-# long-context decode runs at the three split counts its parity test forces.
+# Workloads measured beside the headline one: (name, split counts, fp8 latent
+# cache); the long-context decode runs at the three split counts its parity
+# test forces, and two decode shapes run over the fp8 latent cache as well.
 OTHER_WORKLOADS = (
-    ("decode_b32_l8192", (0,)),
-    ("decode_b8_l131072", (1, 8, 32)),
-    ("prefill_4096_of_65536", (0,)),
-    ("mixed_b64_mtp2", (0,)),
+    ("decode_b32_l8192", (0,), False),
+    ("decode_b8_l131072", (1, 8, 32), False),
+    ("prefill_4096_of_65536", (0,), False),
+    ("mixed_b64_mtp2", (0,), False),
+    ("decode_b32_l8192", (0,), True),
+    ("decode_b8_l131072", (0,), True),
 )
 
 
