@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_b32_l8192")
     ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--kv-fp8", action="store_true", help="run the step over the fp8 latent cache")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clock-load", action="store_true", help="skip the one-second load before the timed steps")
@@ -310,8 +311,8 @@ def main():
         dist.init_process_group("nccl")
     from deepseek_sparse_attention_fp8_gb300.step import DsaStep
 
-    wl = make_workload(args.workload)
-    step = DsaStep(wl, device=f"cuda:{local}", num_kv_splits=args.splits)
+    wl = make_workload(args.workload, kv_fp8=args.kv_fp8)
+    step = DsaStep(wl, device=f"cuda:{local}", num_kv_splits=args.splits, kv_fp8=args.kv_fp8)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=step.device)
     flush_rd = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=step.device)
@@ -455,7 +456,7 @@ def main():
                "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e, "p10_ms": e2e_stats["p10_ms"],
                "p90_ms": e2e_stats["p90_ms"]}
 
-    alg = algorithmic_bytes(wl, step.topk_idx.cpu().numpy())
+    alg = algorithmic_bytes(wl, step.topk_idx.cpu().numpy(), wl.kv_row_bytes_fp8 if args.kv_fp8 else None)
     kern = kernel_table(wl, phase_ms, alg, peaks_doc)
     # bf16 keys read, codes and scales written
     prod_bytes = wl.T * (wl.Di * 2 + wl.Di + 4)
@@ -477,6 +478,7 @@ def main():
         "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "context": int(wl.seq_lens.max()),
                    "index_topk": wl.index_topk, "Hi": wl.Hi, "Di": wl.Di, "H": wl.H, "Dk": wl.Dk, "Dv": wl.Dv,
                    "block_size": wl.block_size, "num_kv_splits": splits_used,
+                   "kv_cache": "fp8 (656 B/row)" if args.kv_fp8 else "bf16",
                    "l2": "flushed between steps (256 MiB write + 256 MiB read)",
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
         "roofline": {"bound": kern[dom]["bound"], "kernel": dom,

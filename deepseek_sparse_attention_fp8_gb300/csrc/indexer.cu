@@ -43,10 +43,23 @@ constexpr int kMaxBlocksPerCta = kMaxTilesPerCta * kTileKeys / 64 + 2;  // block
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// x / s correctly rounded, given y = RN(1/s): q = RN(x y) is within one ulp
+// of x / s, the remainder x - s q is exact in one FMA, and RN(q + (x - s q) y)
+// is the correctly rounded quotient (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990). A zero x is returned as x * y so that -0 keeps its sign.
+__device__ __forceinline__ float div_by_recip(float x, float s, float y) {
+  const float q = x * y;
+  if (q == 0.f) return q;
+  return fmaf(fmaf(-q, s, x), y, q);
+}
+
 // a0 for 16 consecutive dims of one (token, head) row. The row is spread
 // over an aligned group of 8 lanes (lane % 8 = 16-dim chunk, chunks past the
 // head dim hold zeros); the row amax is reduced with shuffles.
-// scale = amax/448 (1 if amax == 0); code = e4m3_rn_satfinite(x / scale).
+// scale = amax/448 (1 if amax == 0); code = e4m3_rn_satfinite(x / scale), the
+// division correctly rounded (by div_by_recip, or IEEE division when 1/scale
+// is not a normal number).
 __device__ __forceinline__ uint4 quant_chunk16(uint4 a, uint4 b, float& scale) {
   const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   float amax = 0.f;
@@ -56,12 +69,23 @@ __device__ __forceinline__ uint4 quant_chunk16(uint4 a, uint4 b, float& scale) {
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
   amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
   scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  const float y = __frcp_rn(scale);
   uint32_t out[4];
+  if (y < 0x1p126f) {  // 1/scale normal (scale is positive): the reciprocal path is exact
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint16_t p0 = cvt_e4m3x2(__fdiv_rn(bf16_lo(u[2 * i]), scale), __fdiv_rn(bf16_hi(u[2 * i]), scale));
-    const uint16_t p1 = cvt_e4m3x2(__fdiv_rn(bf16_lo(u[2 * i + 1]), scale), __fdiv_rn(bf16_hi(u[2 * i + 1]), scale));
-    out[i] = static_cast<uint32_t>(p0) | (static_cast<uint32_t>(p1) << 16);
+    for (int i = 0; i < 4; ++i) {
+      const uint16_t p0 = cvt_e4m3x2(div_by_recip(bf16_lo(u[2 * i]), scale, y), div_by_recip(bf16_hi(u[2 * i]), scale, y));
+      const uint16_t p1 =
+          cvt_e4m3x2(div_by_recip(bf16_lo(u[2 * i + 1]), scale, y), div_by_recip(bf16_hi(u[2 * i + 1]), scale, y));
+      out[i] = static_cast<uint32_t>(p0) | (static_cast<uint32_t>(p1) << 16);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint16_t p0 = cvt_e4m3x2(__fdiv_rn(bf16_lo(u[2 * i]), scale), __fdiv_rn(bf16_hi(u[2 * i]), scale));
+      const uint16_t p1 = cvt_e4m3x2(__fdiv_rn(bf16_lo(u[2 * i + 1]), scale), __fdiv_rn(bf16_hi(u[2 * i + 1]), scale));
+      out[i] = static_cast<uint32_t>(p0) | (static_cast<uint32_t>(p1) << 16);
+    }
   }
   return make_uint4(out[0], out[1], out[2], out[3]);
 }

@@ -52,6 +52,35 @@ def test_quant_q_bit_exact():
         assert np.array_equal(sq.cpu().numpy().view(np.uint32), scales.view(np.uint32))
 
 
+def test_quant_q_bit_exact_across_magnitudes():
+    """a0's division by the scale (a reciprocal with one FMA correction, or
+    IEEE division when 1/scale is not normal) gives the correctly rounded
+    quotient, so the codes equal the oracle's (IEEE fp32 division) bit for
+    bit: rows of every bf16 magnitude from 1e-38 to 1e38, rows with
+    power-of-two scales whose quotients hit e4m3 rounding midpoints exactly,
+    signed zeros and all-zero rows."""
+    rng = np.random.default_rng(11)
+    T, Hi, Di = 512, 16, 128
+    mag = np.exp(rng.uniform(-87, 87, (T, Hi, 1)))  # per-row magnitude
+    x = (rng.standard_normal((T, Hi, Di)) * mag).astype(np.float32)
+    # power-of-two scales: amax = 448 * 2^e, values on and next to e4m3 midpoints
+    e = rng.integers(-20, 20, (T // 4, Hi, 1))
+    mids = np.array([1.0625, 1.1875, 1.3125, 1.4375, 1.5625, 1.6875, 1.8125, 1.9375], np.float32)
+    v = mids[rng.integers(0, 8, (T // 4, Hi, Di))] * np.exp2(rng.integers(-6, 8, (T // 4, Hi, Di)))
+    v *= rng.choice([-1.0, 1.0], v.shape)
+    v[..., 0] = 448.0
+    x[: T // 4] = (v * np.exp2(e)).astype(np.float32)
+    x[T // 4, 0] = 0.0
+    x[T // 4, 1, ::2] = -0.0
+    q = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    q8, sq = api.dsa_quant_q(q)
+    codes, scales = O.quantize_groups(q.float().cpu().numpy())
+    assert np.array_equal(sq.cpu().numpy().view(np.uint32), scales.view(np.uint32))
+    got = q8.cpu().numpy()
+    bad = np.argwhere(got != codes)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[0].tolist()}"
+
+
 def test_indexer_logits(run_small):
     wl, step = run_small
     got = step.logits.cpu().numpy()
