@@ -464,7 +464,7 @@ def main():
                                                   GBps=prod_bytes / (t_prod["ms"] / 1e3) / 1e9)}
     producer["indexer_k_quant_and_cache"]["frac"] = producer["indexer_k_quant_and_cache"]["GBps"] / peak
     dom = max(kern, key=lambda k_: kern[k_]["ms"])
-    traffic = load_traffic(dom, wl.name)
+    traffic = load_traffic(dom, wl.name + ("_fp8kv" if args.kv_fp8 else ""))
     step_bytes = alg["indexer"] + alg["topk"] + alg["attention"]
     launches_per_step = step.kernel_launches()
     splits_used = step.splits
@@ -525,7 +525,7 @@ def main():
                     "step_GBps": obytes / (ts["ms"] / 1e3) / 1e9,
                     "step_frac": obytes / (ts["ms"] / 1e3) / 1e9 / peak,
                     "dominant": odom, "kernels": okern, "phase_sum_ms": osum,
-                    "traffic": load_traffic(odom, name),
+                    "traffic": load_traffic(odom, name + ("_fp8kv" if fp8 else "")) if len(splits_list) == 1 else None,
                 }
                 del ost
                 torch.cuda.empty_cache()
