@@ -100,3 +100,34 @@ def test_decode_b32_l8192_fp8_cache():
     ref, ref_lse = O.sparse_mla(q, kv, wl.kv_block_stride, wl.block_table, wl.seq_lens, wl.query_start_loc, idx,
                                 wl.softmax_scale, wl.Dv, wl.block_size, rows=rows)
     check_attention(step.out.float().cpu().numpy(), ref, np.array(rows), step.lse.cpu().numpy(), ref_lse)
+
+
+@pytest.mark.parametrize("name,rows", [("prefill_4096_of_65536", [0, 2047, 4095]), ("mixed_b64_mtp2", [0, 1, 77, 127])])
+def test_fp8_cache_full_size(name, rows):
+    """The prefill and mixed workloads over the fp8 latent cache, at full size:
+    sampled tokens against the oracle's attention over the decoded cache (the
+    mixed workload's fragmented table leaves NaN-poisoned fp8 blocks unused)."""
+    wl, step = _run(name, kv_fp8=True)
+    idx = step.topk_idx.cpu().numpy()
+    q = bf16_bits_to_float(wl.q)
+    kv = O.mla_fp8_decode_cache(wl.kv_cache_fp8, wl.Dk, wl.Dv)
+    ref, ref_lse = O.sparse_mla(q, kv, wl.kv_block_stride, wl.block_table, wl.seq_lens, wl.query_start_loc, idx,
+                                wl.softmax_scale, wl.Dv, wl.block_size, rows=rows)
+    out = step.out.float().cpu().numpy()
+    assert np.isfinite(out).all()
+    check_attention(out, ref, np.array(rows), step.lse.cpu().numpy(), ref_lse)
+
+
+def test_windowed_topk_full_prefill():
+    """dsa_indexer_topk over 16384-key windows at the full prefill workload
+    (4 windows, a [4096, 16384] logits buffer instead of [4096, 65536]): the
+    selection equals the plain path's, position for position."""
+    from deepseek_sparse_attention_fp8_gb300 import api
+
+    wl, step = _run("prefill_4096_of_65536")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = api.dsa_indexer_topk(step.q_idx, step.w, step.k_cache, step.block_table, step.seq_lens, step.qsl,
+                               wl.block_size, wl.max_q_len, wl.ld, 16384, wl.index_topk, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(got, step.topk_idx)
