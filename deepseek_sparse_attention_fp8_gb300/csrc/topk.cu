@@ -65,6 +65,7 @@ struct TopkShared {
   uint32_t red_u[3][kWarps];
   uint32_t part_ovf[1];              // a warp's candidate list overflowed in this part
   uint32_t bsel, above, thr, gtotal;
+  uint32_t thr_gt;  // threshold-bin elements above the threshold key (row kernel)
   int32_t qsl_s[kThreads + 1], sl_s[kThreads];  // the batch's query_start_loc and seq_lens (B <= kThreads)
 };
 
@@ -133,6 +134,20 @@ __device__ __forceinline__ uint64_t block_exclusive_scan(uint64_t v, uint64_t& t
   const uint64_t r = before_warp + x - v;
   __syncthreads();  // sh.scan is reused by the next call
   return r;
+}
+
+// The block-wide minimum and maximum of the warps' partials in red_f (after
+// a barrier that follows their writes): each warp reduces the 32 partials
+// with shuffles.
+static_assert(kWarps == 32, "one partial per lane");
+__device__ __forceinline__ void block_range(float& lo, float& hi, const TopkShared& sh) {
+  lo = sh.red_f[0][threadIdx.x & 31];
+  hi = sh.red_f[1][threadIdx.x & 31];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
+    hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, off));
+  }
 }
 
 __device__ int valid_length(const int32_t* seq_lens, const int32_t* qsl, int B, int t, int64_t ld, TopkShared& sh) {
@@ -644,13 +659,7 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const TopkParams p) 
   for (int b = tid; b < kBins; b += kThreads) sh.ghist[b] = 0u;
   if (tid == 0) sh.cand_n = 0u;
   __syncthreads();
-  lo = INFINITY;
-  hi = -INFINITY;
-#pragma unroll 8
-  for (int w = 0; w < kWarps; ++w) {
-    lo = fminf(lo, sh.red_f[0][w]);
-    hi = fmaxf(hi, sh.red_f[1][w]);
-  }
+  block_range(lo, hi, sh);
   float inv_w = hi > lo ? static_cast<float>(kBins) / (hi - lo) : 0.f;
   if (!isfinite(inv_w)) inv_w = 0.f;
   if (!(lo <= hi)) lo = 0.f;
@@ -683,16 +692,20 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const TopkParams p) 
     if (tid < static_cast<int>(c)) {
       const uint32_t kk = sh.cand_key[tid];
       const int pos = sh.cand_pos[tid];
-      int rank = 0;
+      int rank = 0, above_kk = 0;
       for (int j = 0; j < static_cast<int>(c); ++j) {
         const uint32_t kj = sh.cand_key[j];
+        above_kk += kj > kk;
         rank += (kj > kk) || (kj == kk && sh.cand_pos[j] < pos);
       }
-      if (rank == need - 1) sh.thr = kk;
+      if (rank == need - 1) {  // exactly one element has this rank
+        sh.thr = kk;
+        sh.thr_gt = static_cast<uint32_t>(above_kk);
+      }
     }
     __syncthreads();
     thr = sh.thr;
-    need -= __syncthreads_count(tid < static_cast<int>(c) && sh.cand_key[tid] > thr);
+    need -= static_cast<int>(sh.thr_gt);
   } else {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
