@@ -210,6 +210,11 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   const int n_cols = p.hi_pad * p.tb;  // MMA N
   const int S = p.stages;
   const int nbuf = 2 * n_cols <= 256 ? 2 : 1;
+  // one token and two accumulators: the two epilogue warp groups take
+  // alternate tiles, each the whole head sum of its keys, so the latency of
+  // one tile's epilogue overlaps the next tile's
+  const bool tile_split = ntok == 1 && nbuf == 2;
+  const int epi_warps = tile_split ? 4 : 8;  // epilogue warps that read one tile
 
   const SmemOffsets so = indexer_smem(n_cols, S);
   uint8_t* sk = smem + so.k;
@@ -329,11 +334,11 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
       if (warp == kProdWarp && lane == 0) {
         for (int s = 0; s < S; ++s) {
           mbar_init(&full_bar[s], DI == 128 ? 1 : 32);
-          mbar_init(&empty_bar[s], 1 + 8);
+          mbar_init(&empty_bar[s], 1 + epi_warps);
         }
         for (int s = 0; s < 2; ++s) {
           mbar_init(&acc_full[s], 1);
-          mbar_init(&acc_empty[s], 8);
+          mbar_init(&acc_empty[s], epi_warps);
         }
         mbar_init(&q_ready, 8);
         for (int q = 0; q < 4; ++q) mbar_init(&pair_bar[q], 2);  // the two warps of a lane group, once per tile
@@ -431,13 +436,15 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
     }
   } else if (n_comp > 0) {
     // ---------------- epilogue: thread = key row = TMEM lane. Warps w and
-    // w+4 share the lanes 32(w%4)..: with two or more tokens they take
-    // alternate tokens; with one token they take half of the heads each and
-    // warp w adds warp w+4's partial sums through shared memory.
+    // w+4 share the lanes 32(w%4)..: with one token and two accumulators they
+    // take alternate tiles (warp group g = w / 4 the tiles i % 2 == g); with
+    // two or more tokens they take alternate tokens of every tile; with one
+    // token and one accumulator they take half of the heads each and warp w
+    // adds warp w+4's partial sums through shared memory.
     const int g = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const bool head_split = ntok == 1 && p.hi_pad % 64 == 0;
+    const bool head_split = !tile_split && ntok == 1 && p.hi_pad % 64 == 0;
     float* part = reinterpret_cast<float*>(smem + so.part);  // [2][128] second-half sums
     // sum over heads [h0, h1) of token j (h1 - h0 a multiple of 16)
     auto head_sum = [&](int buf, int j, int h0, int h1) -> float {
@@ -471,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
       }
       return (a0 + a1) + (a2 + a3);
     };
-    for (int i = 0; i < n_comp && !s_abort; ++i) {
+    for (int i = tile_split ? g : 0; i < n_comp && !s_abort; i += tile_split ? 2 : 1) {
       const int st = i % S, buf = i % nbuf;
       if (!mbar_wait(&acc_full[buf], (i / nbuf) & 1)) {
         if (lane == 0) abort_now();
@@ -484,7 +491,11 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
       const bool bad = s < seq_len && !block_ok(s);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[st]);  // this warp is done with the stage's scales
-      if (head_split) {
+      if (tile_split) {
+        const float acc = head_sum(buf, 0, 0, p.hi_pad);
+        const float out = (s < s_valid[0] && !bad) ? acc * scale_k : -INFINITY;
+        if (col < p.ld) __stcs(p.logits + static_cast<int64_t>(s_tok[0]) * p.ld + col, out);
+      } else if (head_split) {
         const int hh = p.hi_pad / 2;
         const float mine = head_sum(buf, 0, g * hh, (g + 1) * hh);
         float* slot = part + (i & 1) * kTileKeys;
