@@ -446,37 +446,34 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const bool head_split = !tile_split && ntok == 1 && p.hi_pad % 64 == 0;
     float* part = reinterpret_cast<float*>(smem + so.part);  // [2][128] second-half sums
-    // sum over heads [h0, h1) of token j (h1 - h0 a multiple of 16)
+    // sum over heads [h0, h1) of token j (h1 - h0 a multiple of 16): four
+    // independent chains, head h on chain h % 4; chains 0, 1 and chains 2, 3
+    // advance together by one packed FMA each (each lane rounded once, as an
+    // fmaf of its own)
     auto head_sum = [&](int buf, int j, int h0, int h1) -> float {
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // independent FMA chains
+      float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
       const uint32_t col = buf * acc_cols + j * p.hi_pad;
       const float4* w4 = reinterpret_cast<const float4*>(sw + j * p.hi_pad);
+      auto step4 = [&](const float4 w, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+        a01 = __ffma2_rn(make_float2(w.x, w.y),
+                         make_float2(fmaxf(__uint_as_float(v0), 0.f), fmaxf(__uint_as_float(v1), 0.f)), a01);
+        a23 = __ffma2_rn(make_float2(w.z, w.w),
+                         make_float2(fmaxf(__uint_as_float(v2), 0.f), fmaxf(__uint_as_float(v3), 0.f)), a23);
+      };
       for (int hc = h0; hc < h1; hc += 32) {
         if (hc + 32 <= h1) {
           uint32_t v[32];
           tmem_ld32_sync(lane_addr + col + hc, v);
 #pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            const float4 w = w4[hc / 4 + x];
-            a0 = fmaf(w.x, fmaxf(__uint_as_float(v[4 * x]), 0.f), a0);
-            a1 = fmaf(w.y, fmaxf(__uint_as_float(v[4 * x + 1]), 0.f), a1);
-            a2 = fmaf(w.z, fmaxf(__uint_as_float(v[4 * x + 2]), 0.f), a2);
-            a3 = fmaf(w.w, fmaxf(__uint_as_float(v[4 * x + 3]), 0.f), a3);
-          }
+          for (int x = 0; x < 8; ++x) step4(w4[hc / 4 + x], v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
         } else {
           uint32_t v[16];
           tmem_ld16_sync(lane_addr + col + hc, v);
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const float4 w = w4[hc / 4 + x];
-            a0 = fmaf(w.x, fmaxf(__uint_as_float(v[4 * x]), 0.f), a0);
-            a1 = fmaf(w.y, fmaxf(__uint_as_float(v[4 * x + 1]), 0.f), a1);
-            a2 = fmaf(w.z, fmaxf(__uint_as_float(v[4 * x + 2]), 0.f), a2);
-            a3 = fmaf(w.w, fmaxf(__uint_as_float(v[4 * x + 3]), 0.f), a3);
-          }
+          for (int x = 0; x < 4; ++x) step4(w4[hc / 4 + x], v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
         }
       }
-      return (a0 + a1) + (a2 + a3);
+      return (a01.x + a01.y) + (a23.x + a23.y);
     };
     for (int i = tile_split ? g : 0; i < n_comp && !s_abort; i += tile_split ? 2 : 1) {
       const int st = i % S, buf = i % nbuf;

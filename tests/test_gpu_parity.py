@@ -89,6 +89,36 @@ def test_indexer_logits(run_small):
     assert int(step.dev_status.item()) == 0
 
 
+HEAD_SHAPES = {
+    "decode": ("decode_b32_l8192", dict(lens=[700, 1500, 333])),
+    "mtp2": ("mixed_b64_mtp2", dict(lens=[900, 1300, 65])),
+    "prefill": ("prefill_4096_of_65536", dict(L=900, q_len=13)),
+}
+
+
+@pytest.mark.parametrize("Hi,Di", [(64, 128), (48, 128), (16, 128), (64, 64), (32, 64), (64, 32), (48, 32)])
+@pytest.mark.parametrize("shape", sorted(HEAD_SHAPES))
+def test_indexer_logits_head_shapes(shape, Hi, Di):
+    """The logits kernel over indexer head counts (padded to multiples of 16)
+    and head dims 32, 64 and 128 (TMA key pages for 128, 16-byte copies
+    otherwise), for one token per CTA (two accumulators, alternate tiles), two
+    (alternate tokens) and four (one accumulator when the tokens' heads fill
+    more than 128 columns; the 13-token prefill ends in a block of a single
+    token), against the oracle; the top-k of the same logits is exact."""
+    base, kw = HEAD_SHAPES[shape]
+    wl = make_workload(base, Hi=Hi, Di=Di, index_topk=256, **kw)
+    step = DsaStep(wl)
+    step.logits.fill_(float("nan"))  # dirty buffer: every entry must be rewritten
+    step.indexer()
+    step.topk()
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) == 0
+    got = step.logits.cpu().numpy()
+    check_logits(got, oracle_logits(wl), range(wl.T))
+    idx = step.topk_idx.cpu().numpy()
+    check_topk_sets(idx, O.topk(got, wl.seq_lens, wl.query_start_loc, wl.index_topk), range(wl.T))
+
+
 def test_topk_exact_on_same_logits(run_small):
     wl, step = run_small
     logits = step.logits.cpu().numpy()
