@@ -24,7 +24,7 @@
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller. The library
  *     never allocates, frees or synchronises; every call only enqueues kernels
- *     on `stream` (so a sequence of calls can be captured in a CUDA graph).
+ *     on `stream`.
  *   - Arguments are validated on the host before any launch. A bad argument
  *     returns DSA_ERR_INVALID_ARG (or DSA_ERR_UNSUPPORTED for a valid but
  *     unimplemented shape) and launches nothing; dsa_last_error() then holds
