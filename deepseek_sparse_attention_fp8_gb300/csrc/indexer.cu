@@ -449,16 +449,20 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
     // sum over heads [h0, h1) of token j (h1 - h0 a multiple of 16): four
     // independent chains, head h on chain h % 4; chains 0, 1 and chains 2, 3
     // advance together by one packed FMA each (each lane rounded once, as an
-    // fmaf of its own)
+    // fmaf of its own). ReLU(x) is taken as (x + |x|) / 2 on the FMA pipe:
+    // for finite x, x + |x| is exactly 2x or +0, so every chain holds exactly
+    // twice the sum of w * ReLU(x) (scaling by 2 commutes with rounding) and
+    // one halving at the end gives the same bits as max(x, 0) would; a NaN
+    // score (a NaN key code) stays NaN, as in the definition
     auto head_sum = [&](int buf, int j, int h0, int h1) -> float {
       float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
       const uint32_t col = buf * acc_cols + j * p.hi_pad;
       const float4* w4 = reinterpret_cast<const float4*>(sw + j * p.hi_pad);
       auto step4 = [&](const float4 w, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
-        a01 = __ffma2_rn(make_float2(w.x, w.y),
-                         make_float2(fmaxf(__uint_as_float(v0), 0.f), fmaxf(__uint_as_float(v1), 0.f)), a01);
-        a23 = __ffma2_rn(make_float2(w.z, w.w),
-                         make_float2(fmaxf(__uint_as_float(v2), 0.f), fmaxf(__uint_as_float(v3), 0.f)), a23);
+        const float x0 = __uint_as_float(v0), x1 = __uint_as_float(v1), x2 = __uint_as_float(v2),
+                    x3 = __uint_as_float(v3);
+        a01 = __ffma2_rn(make_float2(w.x, w.y), make_float2(x0 + fabsf(x0), x1 + fabsf(x1)), a01);
+        a23 = __ffma2_rn(make_float2(w.z, w.w), make_float2(x2 + fabsf(x2), x3 + fabsf(x3)), a23);
       };
       for (int hc = h0; hc < h1; hc += 32) {
         if (hc + 32 <= h1) {
@@ -473,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
           for (int x = 0; x < 4; ++x) step4(w4[hc / 4 + x], v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
         }
       }
-      return (a01.x + a01.y) + (a23.x + a23.y);
+      return 0.5f * ((a01.x + a01.y) + (a23.x + a23.y));
     };
     for (int i = tile_split ? g : 0; i < n_comp && !s_abort; i += tile_split ? 2 : 1) {
       const int st = i % S, buf = i % nbuf;
