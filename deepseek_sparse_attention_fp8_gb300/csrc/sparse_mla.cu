@@ -875,27 +875,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
 // A thread merges 8 consecutive values of one (token, head) row; a block of
 // 128 threads covers 128 * 8 / DV rows. Launched as a programmatic dependent
 // of the split kernel: it waits for that grid's completion before any read.
+// NS > 0: the split count is NS, and every (m, l) pair and partial value of
+// the thread is loaded before any arithmetic (one round of L2 reads); NS = 0:
+// any split count, split by split. The arithmetic, and so every output bit,
+// is the same in both.
+template <int NS>
 __global__ void __launch_bounds__(128) mla_merge_kernel(const float* __restrict__ o_part,
                                                         const float2* __restrict__ ml, int S, int DV, int64_t n_rows,
                                                         uint16_t* __restrict__ out, float* __restrict__ lse) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if constexpr (NS > 0) S = NS;
   const int tpr = DV / 8;  // threads per row
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (128 / tpr) + threadIdx.x / tpr;
   if (row >= n_rows) return;
   const int v = (threadIdx.x % tpr) * 8;
   const float2* mlr = ml + row * S;
+  const float* orow = o_part + row * S * DV + v;
   float M = kNegSentinel;
-  for (int j = 0; j < S; ++j) M = fmaxf(M, mlr[j].x);
   float den = 0.f;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  const float* orow = o_part + row * S * DV + v;
-#pragma unroll 4
-  for (int j = 0; j < S; ++j) {
-    const float2 mlj = mlr[j];
+  auto add = [&](const float2 mlj, const float4 o0, const float4 o1) {
     const float a = exp2f(mlj.x - M);
     den = fmaf(a, mlj.y, den);
-    const float4 o0 = *reinterpret_cast<const float4*>(orow + static_cast<int64_t>(j) * DV);
-    const float4 o1 = *reinterpret_cast<const float4*>(orow + static_cast<int64_t>(j) * DV + 4);
     acc[0] = fmaf(a, o0.x, acc[0]);
     acc[1] = fmaf(a, o0.y, acc[1]);
     acc[2] = fmaf(a, o0.z, acc[2]);
@@ -904,6 +905,26 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const float* __restrict_
     acc[5] = fmaf(a, o1.y, acc[5]);
     acc[6] = fmaf(a, o1.z, acc[6]);
     acc[7] = fmaf(a, o1.w, acc[7]);
+  };
+  if constexpr (NS > 0) {
+    float2 mlv[NS];
+    float4 o0[NS], o1[NS];
+#pragma unroll
+    for (int j = 0; j < NS; ++j) {
+      mlv[j] = mlr[j];
+      o0[j] = *reinterpret_cast<const float4*>(orow + static_cast<int64_t>(j) * DV);
+      o1[j] = *reinterpret_cast<const float4*>(orow + static_cast<int64_t>(j) * DV + 4);
+    }
+#pragma unroll
+    for (int j = 0; j < NS; ++j) M = fmaxf(M, mlv[j].x);
+#pragma unroll
+    for (int j = 0; j < NS; ++j) add(mlv[j], o0[j], o1[j]);
+  } else {
+    for (int j = 0; j < S; ++j) M = fmaxf(M, mlr[j].x);
+#pragma unroll 4
+    for (int j = 0; j < S; ++j)
+      add(mlr[j], *reinterpret_cast<const float4*>(orow + static_cast<int64_t>(j) * DV),
+          *reinterpret_cast<const float4*>(orow + static_cast<int64_t>(j) * DV + 4));
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   uint4 w;
@@ -915,10 +936,11 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const float* __restrict_
   if (v == 0 && lse != nullptr) lse[row] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
 }
 
-FuncAttrOnce g_smem_merge;
+FuncAttrOnce g_smem_merge[5];
 
-dsa_status_t launch_merge(const MlaParams& p, int Dv, float* lse, cudaStream_t s) {
-  dsa_status_t st = allow_smem(mla_merge_kernel, 0, g_smem_merge);
+template <int NS>
+dsa_status_t launch_merge_ns(const MlaParams& p, int Dv, float* lse, cudaStream_t s, FuncAttrOnce& once) {
+  dsa_status_t st = allow_smem(mla_merge_kernel<NS>, 0, once);
   if (st != DSA_OK) return st;
   const int64_t n_rows = static_cast<int64_t>(p.T) * p.H;
   const int rows_per_block = 128 / (Dv / 8);
@@ -931,10 +953,21 @@ dsa_status_t launch_merge(const MlaParams& p, int Dv, float* lse, cudaStream_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, mla_merge_kernel, static_cast<const float*>(p.o_part),
+  cudaError_t e = cudaLaunchKernelEx(&cfg, mla_merge_kernel<NS>, static_cast<const float*>(p.o_part),
                                      static_cast<const float2*>(p.ml_part), p.splits, Dv, n_rows, p.out, lse);
   if (e != cudaSuccess) return fail(DSA_ERR_CUDA, "mla_merge_kernel launch failed: %s", cudaGetErrorString(e));
   return DSA_OK;
+}
+
+// the split counts the automatic choice gives at decode get their own unrolled merge
+dsa_status_t launch_merge(const MlaParams& p, int Dv, float* lse, cudaStream_t s) {
+  switch (p.splits) {
+    case 2: return launch_merge_ns<2>(p, Dv, lse, s, g_smem_merge[0]);
+    case 3: return launch_merge_ns<3>(p, Dv, lse, s, g_smem_merge[1]);
+    case 4: return launch_merge_ns<4>(p, Dv, lse, s, g_smem_merge[2]);
+    case 8: return launch_merge_ns<8>(p, Dv, lse, s, g_smem_merge[3]);
+    default: return launch_merge_ns<0>(p, Dv, lse, s, g_smem_merge[4]);
+  }
 }
 
 FuncAttrOnce g_smem_big, g_smem_tiny, g_smem_f8;
