@@ -70,7 +70,7 @@ def test_fp8_cache_empty_and_invalid_selection():
     idx[1, :5] = torch.tensor([10**6, -7, 3, 3, 2499], dtype=torch.int32)
     step.topk_idx.copy_(idx)
     step.dev_status.zero_()
-    for splits in (1, 4):
+    for splits in (1, 2, 4):
         step.splits = splits
         step.attention()
         torch.cuda.synchronize()

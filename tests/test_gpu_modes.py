@@ -84,7 +84,7 @@ def test_topk_selection_reused_by_a_second_layer():
     out2 = torch.empty_like(step.out)
     lse2 = torch.empty_like(step.lse)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for splits in (1, 4):
+    for splits in (1, 2, 4):
         api.sparse_mla_decode(q2, kv2, step.block_table, step.seq_lens, step.qsl, idx, wl.softmax_scale, wl.Dv,
                               out2, lse2, num_kv_splits=splits, dev_status=status)
         torch.cuda.synchronize()
