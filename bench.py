@@ -47,6 +47,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_b32_l8192")
+    ap.add_argument("--config", type=int, default=None, metavar="N",
+                    help="workload by configuration index (0 tiny, 1 decode_b32_l8192, 2 decode_b8_l131072, "
+                         "3 prefill_4096_of_65536, 4 mixed_b64_mtp2); overrides --workload")
+    ap.add_argument("--seed", type=int, default=None, help="input seed (default: the workload's own)")
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--kv-fp8", action="store_true", help="run the step over the fp8 latent cache")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -57,7 +61,14 @@ def parse():
                          "'workloads')")
     ap.add_argument("--oracle-seconds", type=int, default=0, metavar="N",
                     help="print the oracle's seconds for N evenly spaced query tokens of the workload and exit (no GPU)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.config is not None:
+        from deepseek_sparse_attention_fp8_gb300.inputs import CONFIG_WORKLOADS
+
+        if not 0 <= args.config < len(CONFIG_WORKLOADS):
+            ap.error(f"--config must be in 0..{len(CONFIG_WORKLOADS) - 1}")
+        args.workload = CONFIG_WORKLOADS[args.config]
+    return args
 
 
 def dist_info():
@@ -290,13 +301,13 @@ def main():
     from deepseek_sparse_attention_fp8_gb300.inputs import make_workload
 
     if args.oracle_seconds:
-        wl = make_workload(args.workload)
+        wl = make_workload(args.workload, seed=args.seed)
         print(cpu_oracle_step(wl, oracle_rows(wl.T, args.oracle_seconds), threads=1), flush=True)
         return
     if args.impl == "reference":
         if rank != 0:
             return
-        run_reference(args, make_workload(args.workload))
+        run_reference(args, make_workload(args.workload, seed=args.seed))
         return
 
     import torch
@@ -311,7 +322,7 @@ def main():
         dist.init_process_group("nccl")
     from deepseek_sparse_attention_fp8_gb300.step import DsaStep
 
-    wl = make_workload(args.workload, kv_fp8=args.kv_fp8)
+    wl = make_workload(args.workload, seed=args.seed, kv_fp8=args.kv_fp8)
     step = DsaStep(wl, device=f"cuda:{local}", num_kv_splits=args.splits, kv_fp8=args.kv_fp8)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=step.device)
@@ -480,6 +491,7 @@ def main():
                    "block_size": wl.block_size, "num_kv_splits": splits_used,
                    "kv_cache": "fp8 (656 B/row)" if args.kv_fp8 else "bf16",
                    "l2": "flushed between steps (256 MiB write + 256 MiB read)",
+                   "seed": "workload default" if args.seed is None else args.seed,
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
         "roofline": {"bound": kern[dom]["bound"], "kernel": dom,
                      "achieved": kern[dom]["GBps"] if kern[dom]["bound"] == "hbm" else kern[dom]["TFLOPs"],

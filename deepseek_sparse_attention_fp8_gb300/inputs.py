@@ -67,6 +67,9 @@ class Workload:
         return int(np.max(np.diff(self.query_start_loc))) if self.B else 0
 
 
+# the five configurations of the benchmark in their fixed order (config 0 .. 4)
+CONFIG_WORKLOADS = ("tiny", "decode_b32_l8192", "decode_b8_l131072", "prefill_4096_of_65536", "mixed_b64_mtp2")
+
 WORKLOADS = {
     # name: (B, L or (lo, hi), q_len, Hi, Di, H, Dk, Dv, topk, kv_std, w_div, table kind, seed)
     "tiny": dict(B=1, L=256, q_len=1, Hi=4, Di=32, H=4, Dk=80, Dv=64, topk=64, kv_std=1.0, table="identity", seed=0),

@@ -13,6 +13,9 @@ caches stay resident in their own buffers.
 """
 from __future__ import annotations
 
+import contextlib
+import os
+
 import numpy as np
 import torch
 
@@ -49,8 +52,22 @@ def _dev(a, dtype, device):
     return t.to(device=device, dtype=dtype) if t.dtype != dtype else t.to(device)
 
 
+def _nvtx_enabled() -> bool:
+    return os.environ.get("DSA_NVTX", "0") not in ("", "0")
+
+
 class DsaStep:
+    """One DSA step over a workload's device buffers: indexer logits (a0 + a1),
+    top-k (a2), sparse MLA with its split merge (a3 + a4).
+
+    num_kv_splits: 0 automatic, -1 batch-invariant (fixed by index_topk), n > 0
+    that many; when 0 and the environment sets DSA_NUM_KV_SPLITS, that value.
+    DSA_NVTX=1 wraps each call in an NVTX range (for profilers)."""
+
     def __init__(self, wl, device="cuda", num_kv_splits: int = 0, prefill: bool | None = None, kv_fp8: bool = False):
+        if num_kv_splits == 0 and os.environ.get("DSA_NUM_KV_SPLITS"):
+            num_kv_splits = int(os.environ["DSA_NUM_KV_SPLITS"])
+        self.nvtx = _nvtx_enabled()
         self.wl = wl
         self.device = torch.device(device)
         d = self.device
@@ -83,15 +100,30 @@ class DsaStep:
         self.ws_topk = torch.empty(max(ws_topk, 16), dtype=torch.uint8, device=d)
         self.ws_mla = torch.empty(max(ws_mla, 16), dtype=torch.uint8, device=d)
 
+    def _range(self, name):
+        return torch.cuda.nvtx.range(name) if self.nvtx else contextlib.nullcontext()
+
     def indexer(self, stream=None):
+        with self._range("dsa_indexer_logits"):
+            self._indexer(stream)
+
+    def topk(self, stream=None):
+        with self._range("dsa_topk"):
+            self._topk(stream)
+
+    def attention(self, stream=None):
+        with self._range("sparse_mla"):
+            self._attention(stream)
+
+    def _indexer(self, stream=None):
         wl = self.wl
         api.dsa_indexer_logits(self.q_idx, self.w, self.k_cache, self.block_table, self.seq_lens, self.qsl,
                                wl.block_size, wl.max_q_len, self.logits, self.dev_status, stream)
 
-    def topk(self, stream=None):
+    def _topk(self, stream=None):
         api.dsa_topk(self.logits, self.seq_lens, self.qsl, self.wl.index_topk, self.topk_idx, self.ws_topk, stream)
 
-    def attention(self, stream=None):
+    def _attention(self, stream=None):
         wl = self.wl
         prefill = api.sparse_mla_prefill_fp8 if self.kv_fp8 else api.sparse_mla_prefill
         decode = api.sparse_mla_decode_fp8 if self.kv_fp8 else api.sparse_mla_decode

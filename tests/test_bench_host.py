@@ -39,3 +39,20 @@ def test_oracle_sample_is_bounded_and_evenly_spaced():
 def test_cpu_model_names_the_host():
     name = bench.cpu_model()
     assert isinstance(name, str) and name.strip()
+
+
+def test_config_index_selects_the_workload(monkeypatch):
+    from deepseek_sparse_attention_fp8_gb300.inputs import CONFIG_WORKLOADS, WORKLOADS
+
+    assert set(CONFIG_WORKLOADS) == set(WORKLOADS)
+    for n, name in enumerate(CONFIG_WORKLOADS):
+        monkeypatch.setattr(sys, "argv", ["bench.py", "--config", str(n), "--seed", "7"])
+        args = bench.parse()
+        assert args.workload == name and args.seed == 7
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--config", "5"])
+    try:
+        bench.parse()
+    except SystemExit:
+        pass
+    else:
+        raise AssertionError("an out-of-range --config must be refused")

@@ -114,3 +114,14 @@ def test_attention_with_large_scores(q_std, splits):
     idx = step.topk_idx.cpu().numpy()
     ref, ref_lse = oracle_attention(wl, idx)
     check_attention(step.out.float().cpu().numpy(), ref, np.arange(wl.T), step.lse.cpu().numpy(), ref_lse)
+
+
+def test_split_count_from_the_environment(monkeypatch):
+    """DSA_NUM_KV_SPLITS sets the split count of a step built with the
+    automatic count; an explicit count keeps precedence."""
+    wl = make_workload("decode_b32_l8192", B=3, lens=[1000, 2500, 777], index_topk=2048)
+    monkeypatch.setenv("DSA_NUM_KV_SPLITS", "4")
+    assert DsaStep(wl).splits == 4
+    assert DsaStep(wl, num_kv_splits=2).splits == 2
+    monkeypatch.delenv("DSA_NUM_KV_SPLITS")
+    assert DsaStep(wl).splits == api.sparse_mla_num_splits(wl.T, wl.H, wl.Dv, wl.index_topk, 0)
