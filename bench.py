@@ -1,14 +1,15 @@
 """Benchmark of one DSA step (indexer logits -> top-k -> sparse MLA + merge).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--splits S]
+                    [--workload NAME | --config N] [--splits S] [--seed S] [--kv-fp8]
 
 Default workload: decode_b32_l8192 (32 requests x 1 query token, 8192 cached
 tokens each, 64x128 fp8 indexer, top-2048, 128-head 576/512 MLA). Prints one
 JSON line. `value` is decode tokens/s over the device-timed step with inputs
 resident in HBM and L2 flushed between steps; `e2e` repeats it through the
-public API with per-step inputs copied from pinned host memory and the output
-read back. Times are medians over the timed steps (p10 / p90 beside them).
+public API with per-step inputs copied from pinned host memory (the attention
+queries on a side stream while the indexer and top-k run) and the output read
+back. Times are medians over the timed steps (p10 / p90 beside them).
 `kernels` times each phase alone (medians; their sum must stay within 1.3x of
 the step median), `roofline` relates the dominant one to its peak (HBM at
 decode, the e4m3 or bf16 tensor peak at prefill), `workloads` repeats the
@@ -442,13 +443,14 @@ def main():
     # e2e through the public API with host buffers: per-step inputs (queries,
     # head weights, block table, lengths) copied from pinned memory, output and
     # lse read back; the caches stay resident like a serving engine's KV cache.
-    # The step keeps its per-step inputs in one buffer and its outputs in
-    # another, so each direction is one copy.
+    # DsaStep.run_host copies the indexer's inputs first and the attention
+    # queries on a side stream while the indexer and top-k run.
     e2e = None
     if not args.no_e2e:
         host_in = step.inputs.cpu().pin_memory()
+        host_q = step.inputs_q.cpu().pin_memory()
         host_out = torch.empty_like(step.outputs, device="cpu").pin_memory()
-        h2d = host_in.numel() * host_in.element_size()
+        h2d = host_in.numel() * host_in.element_size() + host_q.numel() * host_q.element_size()
         d2h = host_out.numel() * host_out.element_size()
         Ke = max(10, min(K, 200))
         eve = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
@@ -456,9 +458,7 @@ def main():
         for k in range(Ke):
             flush_l2()
             eve[k][0].record(stream)
-            step.inputs.copy_(host_in, non_blocking=True)
-            step.run()
-            host_out.copy_(step.outputs, non_blocking=True)
+            step.run_host(host_in, host_q, host_out)
             eve[k][1].record(stream)
         barrier()
         e2e_stats = summary([e[0].elapsed_time(e[1]) for e in eve])

@@ -71,12 +71,18 @@ class DsaStep:
         self.wl = wl
         self.device = torch.device(device)
         d = self.device
-        ins = [(wl.q_idx, torch.bfloat16), (wl.w, torch.float32), (wl.q, torch.bfloat16),
-               (wl.block_table, torch.int32), (wl.seq_lens, torch.int32), (wl.query_start_loc, torch.int32)]
+        # per-step inputs in two buffers: what the indexer and top-k read, and
+        # the attention queries (copied from the host in parallel with those
+        # kernels by run_host)
+        ins = [(wl.q_idx, torch.bfloat16), (wl.w, torch.float32), (wl.block_table, torch.int32),
+               (wl.seq_lens, torch.int32), (wl.query_start_loc, torch.int32)]
         self.inputs, views = _packed([(np.shape(a), dt) for a, dt in ins], d)
         for v, (a, dt) in zip(views, ins):
             v.copy_(_host(a, dt))
-        self.q_idx, self.w, self.q, self.block_table, self.seq_lens, self.qsl = views
+        self.q_idx, self.w, self.block_table, self.seq_lens, self.qsl = views
+        self.inputs_q, (self.q,) = _packed([(np.shape(wl.q), torch.bfloat16)], d)
+        self.q.copy_(_host(wl.q, torch.bfloat16))
+        self._side = None
         self.k_cache = _dev(wl.k_cache, torch.uint8, d)
         # the latent cache: bf16 rows, or (kv_fp8) the workload's fp8 rows
         self.kv_fp8 = kv_fp8
@@ -139,6 +145,28 @@ class DsaStep:
         self.topk(stream)
         self.attention(stream)
         return self.out
+
+    def run_host(self, host_inputs, host_q, host_outputs):
+        """One step from pinned host memory on the current stream: the
+        indexer's inputs (`host_inputs`, laid out like `inputs`) are copied
+        first; the attention queries (`host_q`, like `inputs_q`) are copied on
+        a side stream while the indexer and top-k run; out and lse come back
+        into `host_outputs` (like `outputs`)."""
+        main = torch.cuda.current_stream(self.device)
+        if self._side is None:
+            self._side = torch.cuda.Stream(self.device)
+            self._q_copied = torch.cuda.Event()
+        self._side.wait_stream(main)  # the previous step's attention has read q
+        with torch.cuda.stream(self._side):
+            self.inputs_q.copy_(host_q, non_blocking=True)
+            self._q_copied.record(self._side)
+        self.inputs.copy_(host_inputs, non_blocking=True)
+        self.indexer()
+        self.topk()
+        main.wait_event(self._q_copied)
+        self.attention()
+        host_outputs.copy_(self.outputs, non_blocking=True)
+        return host_outputs
 
     def kernel_launches(self) -> int:
         """Kernels one run() enqueues."""
