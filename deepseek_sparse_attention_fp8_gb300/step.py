@@ -5,10 +5,12 @@ logits and workspace buffers, so that `run()` only enqueues the library's
 kernels (no allocation, no host synchronisation). It is the call a user
 makes per attention layer and batch; the tests and the benchmark drive it.
 
-The per-step inputs (q_idx, w, q, block_table, seq_lens, query_start_loc)
-are views into one device buffer, `inputs`, and the outputs (out, lse) into
-another, `outputs`, each tensor at a 256-byte aligned offset: a caller that
-stages a step's inputs in host memory moves them with one copy each way. The
+The per-step inputs the indexer and top-k read (q_idx, w, block_table,
+seq_lens, query_start_loc) are views into one device buffer, `inputs`; the
+attention queries q into a second, `inputs_q`; the outputs (out, lse) into a
+third, `outputs`; each tensor at a 256-byte aligned offset. A caller that
+stages a step's inputs in host memory moves them with one copy per buffer
+(`run_host` overlaps the queries' copy with the indexer and top-k). The
 caches stay resident in their own buffers.
 """
 from __future__ import annotations
