@@ -154,3 +154,17 @@ def test_step_from_host_buffers_matches_the_resident_step():
     torch.cuda.synchronize()
     assert torch.equal(got, step.outputs.cpu())
     assert int(step.dev_status.item()) == 0
+
+
+def test_nvtx_ranges_leave_results_unchanged(monkeypatch):
+    """DSA_NVTX=1 wraps each call in an NVTX range; the step's results are the
+    same bits as without."""
+    wl = make_workload("decode_b32_l8192", B=3, lens=[1000, 2500, 777], index_topk=2048)
+    plain = DsaStep(wl)
+    plain.run()
+    monkeypatch.setenv("DSA_NVTX", "1")
+    marked = DsaStep(wl)
+    assert marked.nvtx
+    marked.run()
+    torch.cuda.synchronize()
+    assert torch.equal(plain.outputs, marked.outputs) and torch.equal(plain.topk_idx, marked.topk_idx)
