@@ -209,12 +209,24 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   const int n_comp = max(0, t_comp_end - t_begin);
   const int n_cols = p.hi_pad * p.tb;  // MMA N
   const int S = p.stages;
-  const int nbuf = 2 * n_cols <= 256 ? 2 : 1;
+  // MMA units: a unit is one MMA of a key tile against unit_cols query
+  // columns into one of nbuf accumulators. When all the CTA's columns fit
+  // twice in its 256 TMEM columns, a unit is the whole tile (nbuf = 2). With
+  // three or four tokens of 64 heads they fit once, so a unit is one pair of
+  // tokens: the key tile stays for both pairs and one pair's epilogue overlaps
+  // the next pair's MMA, which a single 256-column accumulator would serialise.
+  const bool pair_split = p.hi_pad == 64 && p.tb > 2;
+  const int n_units = pair_split ? (ntok + 1) / 2 : 1;  // MMA units per key tile
+  const int unit_cols = pair_split ? 2 * p.hi_pad : n_cols;
+  const int nbuf = 2 * unit_cols <= 256 ? 2 : 1;
   // one token and two accumulators: the two epilogue warp groups take
   // alternate tiles, each the whole head sum of its keys, so the latency of
   // one tile's epilogue overlaps the next tile's
-  const bool tile_split = ntok == 1 && nbuf == 2;
-  const int epi_warps = tile_split ? 4 : 8;  // epilogue warps that read one tile
+  const bool tile_split = !pair_split && ntok == 1 && nbuf == 2;
+  // epilogue warps that read one tile's scales: with token pairs the two warp
+  // groups take alternate units (both of a tile when it has two)
+  const int epi_warps = pair_split ? 4 * n_units : (tile_split ? 4 : 8);
+  const int acc_release = pair_split ? 4 : epi_warps;  // warps that release one accumulator
 
   const SmemOffsets so = indexer_smem(n_cols, S);
   uint8_t* sk = smem + so.k;
@@ -229,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   if (tid == 0) s_abort = 0;
 
   uint32_t tmem = 0;
-  const uint32_t acc_cols = n_cols <= 32 ? 32 : (n_cols <= 64 ? 64 : (n_cols <= 128 ? 128 : 256));
+  const uint32_t acc_cols = unit_cols <= 32 ? 32 : (unit_cols <= 64 ? 64 : (unit_cols <= 128 ? 128 : 256));
   const uint32_t tmem_cols = acc_cols * nbuf;
   auto abort_now = [&](void) {
     s_abort = 1;
@@ -338,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
         }
         for (int s = 0; s < 2; ++s) {
           mbar_init(&acc_full[s], 1);
-          mbar_init(&acc_empty[s], epi_warps);
+          mbar_init(&acc_empty[s], acc_release);
         }
         mbar_init(&q_ready, 8);
         for (int q = 0; q < 4; ++q) mbar_init(&pair_bar[q], 2);  // the two warps of a lane group, once per tile
@@ -412,27 +424,32 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
     }
   } else if (n_comp > 0 && warp == kMmaWarp) {
     // ---------------- MMA issuer
-    const uint32_t idesc = idesc_e4m3(128, n_cols);
+    const uint32_t idesc = idesc_e4m3(128, unit_cols);
     if (!mbar_wait(&q_ready, 0) && lane == 0) abort_now();
     for (int i = 0; i < n_comp && !s_abort; ++i) {
-      const int st = i % S, buf = i % nbuf;
+      const int st = i % S;
       bool ok = mbar_wait(&full_bar[st], (i / S) & 1);
-      if (ok && i >= nbuf) ok = mbar_wait(&acc_empty[buf], ((i / nbuf) - 1) & 1);
+      for (int pp = 0; ok && pp < n_units; ++pp) {
+        const int u = i * n_units + pp, buf = u % nbuf;
+        if (u >= nbuf) ok = mbar_wait(&acc_empty[buf], ((u / nbuf) - 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          // unit pp takes the query rows pp * unit_cols.. (whole 1024-byte swizzle atoms)
+          const uint32_t a0 = smem_u32(sk + st * kTileBytes), b0 = smem_u32(sq + pp * unit_cols * 128);
+#pragma unroll
+          for (int ks = 0; ks < DI / 32; ++ks)
+            mma_e4m3_ss(tmem + buf * acc_cols, smem_desc(a0 + ks * 32, 16, 1024, kSwizzle128B),
+                        smem_desc(b0 + ks * 32, 16, 1024, kSwizzle128B), idesc, ks > 0 ? 1u : 0u);
+          if (pp == n_units - 1) mma_commit(&empty_bar[st]);  // the tile's last MMA has read the stage
+          mma_commit(&acc_full[buf]);
+        }
+        __syncwarp();
+      }
       if (!ok) {
         if (lane == 0) abort_now();
         break;
       }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t a0 = smem_u32(sk + st * kTileBytes), b0 = smem_u32(sq);
-#pragma unroll
-        for (int ks = 0; ks < DI / 32; ++ks)
-          mma_e4m3_ss(tmem + buf * acc_cols, smem_desc(a0 + ks * 32, 16, 1024, kSwizzle128B),
-                      smem_desc(b0 + ks * 32, 16, 1024, kSwizzle128B), idesc, ks > 0 ? 1u : 0u);
-        mma_commit(&empty_bar[st]);
-        mma_commit(&acc_full[buf]);
-      }
-      __syncwarp();
     }
   } else if (n_comp > 0) {
     // ---------------- epilogue: thread = key row = TMEM lane. Warps w and
@@ -454,9 +471,8 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
     // twice the sum of w * ReLU(x) (scaling by 2 commutes with rounding) and
     // one halving at the end gives the same bits as max(x, 0) would; a NaN
     // score (a NaN key code) stays NaN, as in the definition
-    auto head_sum = [&](int buf, int j, int h0, int h1) -> float {
+    auto head_sum = [&](uint32_t col, int j, int h0, int h1) -> float {  // token j's heads from TMEM column col
       float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
-      const uint32_t col = buf * acc_cols + j * p.hi_pad;
       const float4* w4 = reinterpret_cast<const float4*>(sw + j * p.hi_pad);
       auto step4 = [&](const float4 w, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
         const float x0 = __uint_as_float(v0), x1 = __uint_as_float(v1), x2 = __uint_as_float(v2),
@@ -479,7 +495,39 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
       }
       return 0.5f * ((a01.x + a01.y) + (a23.x + a23.y));
     };
-    for (int i = tile_split ? g : 0; i < n_comp && !s_abort; i += tile_split ? 2 : 1) {
+    // token pairs: warp group g takes the units u = g, g + 2, .. (with two
+    // pairs per tile, pair g of every tile, always in accumulator g), each
+    // warp both tokens of the pair for its 32 keys, so one group's epilogue
+    // runs while the other's accumulator is refilled; the accumulator goes
+    // back to the MMA before the logits are stored
+    for (int u = g; pair_split && u < n_comp * n_units && !s_abort; u += 2) {
+      const int i = u / n_units, pp = u - i * n_units, buf = u & 1, st = i % S;
+      if (!mbar_wait(&acc_full[buf], (u >> 1) & 1)) {
+        if (lane == 0) abort_now();
+        break;
+      }
+      tc_fence_after();
+      const int col = (t_begin + i) * kTileKeys + r;  // logits column of this lane's key
+      const int s = kb + col;
+      const float scale_k = ssc[st * kTileKeys + r];
+      const bool bad = s < seq_len && !block_ok(s);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[st]);  // this warp is done with the stage's scales
+      const int j0 = 2 * pp, j1 = j0 + 1;
+      const float acc0 = head_sum(buf * acc_cols, j0, 0, 64);
+      const float acc1 = j1 < ntok ? head_sum(buf * acc_cols + 64, j1, 0, 64) : 0.f;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      if (col < p.ld) {
+        __stcs(p.logits + static_cast<int64_t>(s_tok[j0]) * p.ld + col,
+               (s < s_valid[j0] && !bad) ? acc0 * scale_k : -INFINITY);
+        if (j1 < ntok)
+          __stcs(p.logits + static_cast<int64_t>(s_tok[j1]) * p.ld + col,
+                 (s < s_valid[j1] && !bad) ? acc1 * scale_k : -INFINITY);
+      }
+    }
+    for (int i = tile_split ? g : 0; !pair_split && i < n_comp && !s_abort; i += tile_split ? 2 : 1) {
       const int st = i % S, buf = i % nbuf;
       if (!mbar_wait(&acc_full[buf], (i / nbuf) & 1)) {
         if (lane == 0) abort_now();
@@ -493,12 +541,12 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[st]);  // this warp is done with the stage's scales
       if (tile_split) {
-        const float acc = head_sum(buf, 0, 0, p.hi_pad);
+        const float acc = head_sum(buf * acc_cols, 0, 0, p.hi_pad);
         const float out = (s < s_valid[0] && !bad) ? acc * scale_k : -INFINITY;
         if (col < p.ld) __stcs(p.logits + static_cast<int64_t>(s_tok[0]) * p.ld + col, out);
       } else if (head_split) {
         const int hh = p.hi_pad / 2;
-        const float mine = head_sum(buf, 0, g * hh, (g + 1) * hh);
+        const float mine = head_sum(buf * acc_cols, 0, g * hh, (g + 1) * hh);
         float* slot = part + (i & 1) * kTileKeys;
         if (g == 1) slot[r] = mine;
         __syncwarp();
@@ -515,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
         }
       } else {
         for (int j = g; j < ntok; j += 2) {  // one token: warp w alone (fewer than 64 head columns)
-          const float acc = head_sum(buf, j, 0, p.hi_pad);
+          const float acc = head_sum(buf * acc_cols + j * p.hi_pad, j, 0, p.hi_pad);
           const float out = (s < s_valid[j] && !bad) ? acc * scale_k : -INFINITY;
           if (col < p.ld) __stcs(p.logits + static_cast<int64_t>(s_tok[j]) * p.ld + col, out);
         }

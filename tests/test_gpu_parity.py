@@ -93,6 +93,8 @@ HEAD_SHAPES = {
     "decode": ("decode_b32_l8192", dict(lens=[700, 1500, 333])),
     "mtp2": ("mixed_b64_mtp2", dict(lens=[900, 1300, 65])),
     "prefill": ("prefill_4096_of_65536", dict(L=900, q_len=13)),
+    "prefill14": ("prefill_4096_of_65536", dict(L=900, q_len=14)),
+    "prefill15": ("prefill_4096_of_65536", dict(L=900, q_len=15)),
 }
 
 
@@ -103,8 +105,10 @@ def test_indexer_logits_head_shapes(shape, Hi, Di):
     and head dims 32, 64 and 128 (TMA key pages for 128, 16-byte copies
     otherwise), for one token per CTA (two accumulators, alternate tiles), two
     (alternate tokens) and four (one accumulator when the tokens' heads fill
-    more than 128 columns; the 13-token prefill ends in a block of a single
-    token), against the oracle; the top-k of the same logits is exact."""
+    more than 128 columns, or, with 64 heads, one MMA per token pair into two
+    accumulators); the 13-, 14- and 15-token prefills end in a block of one,
+    two and three tokens. Checked against the oracle; the top-k of the same
+    logits is exact."""
     base, kw = HEAD_SHAPES[shape]
     wl = make_workload(base, Hi=Hi, Di=Di, index_topk=256, **kw)
     step = DsaStep(wl)
