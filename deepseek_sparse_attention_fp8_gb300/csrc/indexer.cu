@@ -137,7 +137,7 @@ struct IndexerParams {
 };
 
 struct SmemOffsets {
-  int k, sc, q, w, part, total;
+  int k, sc, q, w, total;
 };
 __host__ __device__ inline SmemOffsets indexer_smem(int n_cols, int stages) {
   SmemOffsets o;
@@ -145,8 +145,7 @@ __host__ __device__ inline SmemOffsets indexer_smem(int n_cols, int stages) {
   o.sc = o.k + stages * kTileBytes;
   o.q = (o.sc + stages * kTileKeys * 4 + 1023) & ~1023;
   o.w = o.q + n_cols * 128;
-  o.part = o.w + n_cols * 4;
-  o.total = o.part + 2 * kTileKeys * 4 + 1024;  // + slack for 1024-byte alignment of the base
+  o.total = o.w + n_cols * 4 + 1024;  // + slack for 1024-byte alignment of the base
   return o;
 }
 // two CTAs per SM: stages sized so that 2 x smem stays within 228 KB
@@ -160,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
                                                                      const __grid_constant__ CUtensorMap kmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], acc_full[2], acc_empty[2], q_ready, pair_bar[4];
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], acc_full[2], acc_empty[2], q_ready;
   __shared__ uint32_t tmem_holder;
   __shared__ int s_tok[kMaxTokensPerCta];
   __shared__ int s_valid[kMaxTokensPerCta];
@@ -222,11 +221,14 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   // one token and two accumulators: the two epilogue warp groups take
   // alternate tiles, each the whole head sum of its keys, so the latency of
   // one tile's epilogue overlaps the next tile's
-  const bool tile_split = !pair_split && ntok == 1 && nbuf == 2;
-  // epilogue warps that read one tile's scales: with token pairs the two warp
-  // groups take alternate units (both of a tile when it has two)
-  const int epi_warps = pair_split ? 4 * n_units : (tile_split ? 4 : 8);
-  const int acc_release = pair_split ? 4 : epi_warps;  // warps that release one accumulator
+  // with two accumulators the two epilogue warp groups take alternate units
+  // (each warp every token of its unit), so one group's head sums run while
+  // the other group's accumulator is refilled; with one accumulator both
+  // groups take alternate tokens of every tile
+  const bool alt_units = nbuf == 2;
+  // epilogue warps that read one tile's scales (two groups when a tile has two units)
+  const int epi_warps = alt_units ? 4 * n_units : 8;
+  const int acc_release = alt_units ? 4 : 8;  // warps that release one accumulator
 
   const SmemOffsets so = indexer_smem(n_cols, S);
   uint8_t* sk = smem + so.k;
@@ -353,7 +355,6 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
           mbar_init(&acc_empty[s], acc_release);
         }
         mbar_init(&q_ready, 8);
-        for (int q = 0; q < 4; ++q) mbar_init(&pair_bar[q], 2);  // the two warps of a lane group, once per tile
         fence_mbar_init();
         // the tile's block ids were stored by this warp (its first 32 entries
         // cover the first 16 tiles: block_size >= 64)
@@ -453,16 +454,11 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
     }
   } else if (n_comp > 0) {
     // ---------------- epilogue: thread = key row = TMEM lane. Warps w and
-    // w+4 share the lanes 32(w%4)..: with one token and two accumulators they
-    // take alternate tiles (warp group g = w / 4 the tiles i % 2 == g); with
-    // two or more tokens they take alternate tokens of every tile; with one
-    // token and one accumulator they take half of the heads each and warp w
-    // adds warp w+4's partial sums through shared memory.
+    // w+4 (warp group g = w / 4) share the lanes 32(w%4)..: with two
+    // accumulators they take alternate units, with one alternate tokens.
     const int g = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const bool head_split = !tile_split && ntok == 1 && p.hi_pad % 64 == 0;
-    float* part = reinterpret_cast<float*>(smem + so.part);  // [2][128] second-half sums
     // sum over heads [h0, h1) of token j (h1 - h0 a multiple of 16): four
     // independent chains, head h on chain h % 4; chains 0, 1 and chains 2, 3
     // advance together by one packed FMA each (each lane rounded once, as an
@@ -495,12 +491,11 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
       }
       return 0.5f * ((a01.x + a01.y) + (a23.x + a23.y));
     };
-    // token pairs: warp group g takes the units u = g, g + 2, .. (with two
-    // pairs per tile, pair g of every tile, always in accumulator g), each
-    // warp both tokens of the pair for its 32 keys, so one group's epilogue
-    // runs while the other's accumulator is refilled; the accumulator goes
-    // back to the MMA before the logits are stored
-    for (int u = g; pair_split && u < n_comp * n_units && !s_abort; u += 2) {
+    // two accumulators: group g takes the units u = g, g + 2, .. (with two
+    // token pairs per tile, pair g of every tile in accumulator g; otherwise
+    // alternate tiles), every token of the unit; the accumulator goes back to
+    // the MMA before the unit's last logits are stored
+    for (int u = g; alt_units && u < n_comp * n_units && !s_abort; u += 2) {
       const int i = u / n_units, pp = u - i * n_units, buf = u & 1, st = i % S;
       if (!mbar_wait(&acc_full[buf], (u >> 1) & 1)) {
         if (lane == 0) abort_now();
@@ -513,23 +508,39 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
       const bool bad = s < seq_len && !block_ok(s);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[st]);  // this warp is done with the stage's scales
-      const int j0 = 2 * pp, j1 = j0 + 1;
-      const float acc0 = head_sum(buf * acc_cols, j0, 0, 64);
-      const float acc1 = j1 < ntok ? head_sum(buf * acc_cols + 64, j1, 0, 64) : 0.f;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
-      if (col < p.ld) {
-        __stcs(p.logits + static_cast<int64_t>(s_tok[j0]) * p.ld + col,
-               (s < s_valid[j0] && !bad) ? acc0 * scale_k : -INFINITY);
-        if (j1 < ntok)
-          __stcs(p.logits + static_cast<int64_t>(s_tok[j1]) * p.ld + col,
-                 (s < s_valid[j1] && !bad) ? acc1 * scale_k : -INFINITY);
+      if (pair_split) {  // 64 heads: constant trip counts
+        const int j0 = 2 * pp, j1 = j0 + 1;
+        const float acc0 = head_sum(buf * acc_cols, j0, 0, 64);
+        const float acc1 = j1 < ntok ? head_sum(buf * acc_cols + 64, j1, 0, 64) : 0.f;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        if (col < p.ld) {
+          __stcs(p.logits + static_cast<int64_t>(s_tok[j0]) * p.ld + col,
+                 (s < s_valid[j0] && !bad) ? acc0 * scale_k : -INFINITY);
+          if (j1 < ntok)
+            __stcs(p.logits + static_cast<int64_t>(s_tok[j1]) * p.ld + col,
+                   (s < s_valid[j1] && !bad) ? acc1 * scale_k : -INFINITY);
+        }
+        continue;
+      }
+      for (int j = 0; j < ntok; ++j) {
+        const float acc = head_sum(buf * acc_cols + j * p.hi_pad, j, 0, p.hi_pad);
+        if (j + 1 == ntok) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+        if (col < p.ld)
+          __stcs(p.logits + static_cast<int64_t>(s_tok[j]) * p.ld + col,
+                 (s < s_valid[j] && !bad) ? acc * scale_k : -INFINITY);
       }
     }
-    for (int i = tile_split ? g : 0; !pair_split && i < n_comp && !s_abort; i += tile_split ? 2 : 1) {
-      const int st = i % S, buf = i % nbuf;
-      if (!mbar_wait(&acc_full[buf], (i / nbuf) & 1)) {
+    // one accumulator (more than 128 columns of fewer than 64 heads): both
+    // groups read every tile, warp w the tokens g, g + 2, ..
+    for (int i = 0; !alt_units && i < n_comp && !s_abort; ++i) {
+      const int st = i % S;
+      if (!mbar_wait(&acc_full[0], i & 1)) {
         if (lane == 0) abort_now();
         break;
       }
@@ -540,37 +551,15 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
       const bool bad = s < seq_len && !block_ok(s);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[st]);  // this warp is done with the stage's scales
-      if (tile_split) {
-        const float acc = head_sum(buf * acc_cols, 0, 0, p.hi_pad);
-        const float out = (s < s_valid[0] && !bad) ? acc * scale_k : -INFINITY;
-        if (col < p.ld) __stcs(p.logits + static_cast<int64_t>(s_tok[0]) * p.ld + col, out);
-      } else if (head_split) {
-        const int hh = p.hi_pad / 2;
-        const float mine = head_sum(buf * acc_cols, 0, g * hh, (g + 1) * hh);
-        float* slot = part + (i & 1) * kTileKeys;
-        if (g == 1) slot[r] = mine;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pair_bar[warp & 3]);
-        // both warps arrive once per tile, so neither runs two tiles ahead
-        if (g == 0 && !mbar_wait(&pair_bar[warp & 3], i & 1)) {
-          if (lane == 0) abort_now();
-          break;
-        }
-        if (g == 0) {
-          const float acc = mine + slot[r];
-          const float out = (s < s_valid[0] && !bad) ? acc * scale_k : -INFINITY;
-          if (col < p.ld) __stcs(p.logits + static_cast<int64_t>(s_tok[0]) * p.ld + col, out);
-        }
-      } else {
-        for (int j = g; j < ntok; j += 2) {  // one token: warp w alone (fewer than 64 head columns)
-          const float acc = head_sum(buf * acc_cols + j * p.hi_pad, j, 0, p.hi_pad);
-          const float out = (s < s_valid[j] && !bad) ? acc * scale_k : -INFINITY;
-          if (col < p.ld) __stcs(p.logits + static_cast<int64_t>(s_tok[j]) * p.ld + col, out);
-        }
+      for (int j = g; j < ntok; j += 2) {
+        const float acc = head_sum(j * p.hi_pad, j, 0, p.hi_pad);
+        if (col < p.ld)
+          __stcs(p.logits + static_cast<int64_t>(s_tok[j]) * p.ld + col,
+                 (s < s_valid[j] && !bad) ? acc * scale_k : -INFINITY);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      if (lane == 0) mbar_arrive(&acc_empty[0]);
     }
   }
 

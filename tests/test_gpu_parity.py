@@ -103,12 +103,12 @@ HEAD_SHAPES = {
 def test_indexer_logits_head_shapes(shape, Hi, Di):
     """The logits kernel over indexer head counts (padded to multiples of 16)
     and head dims 32, 64 and 128 (TMA key pages for 128, 16-byte copies
-    otherwise), for one token per CTA (two accumulators, alternate tiles), two
-    (alternate tokens) and four (one accumulator when the tokens' heads fill
-    more than 128 columns, or, with 64 heads, one MMA per token pair into two
-    accumulators); the 13-, 14- and 15-token prefills end in a block of one,
-    two and three tokens. Checked against the oracle; the top-k of the same
-    logits is exact."""
+    otherwise), for one, two and four tokens per CTA: two accumulators taken
+    by the two epilogue warp groups in turn (whole tiles, or token pairs for
+    three or four tokens of 64 heads), or one accumulator read by both groups
+    when fewer than 64 heads of four tokens fill more than 128 columns; the
+    13-, 14- and 15-token prefills end in a block of one, two and three
+    tokens. Checked against the oracle; the top-k of the same logits is exact."""
     base, kw = HEAD_SHAPES[shape]
     wl = make_workload(base, Hi=Hi, Di=Di, index_topk=256, **kw)
     step = DsaStep(wl)
