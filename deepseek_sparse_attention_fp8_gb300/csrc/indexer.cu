@@ -492,48 +492,60 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
       return 0.5f * ((a01.x + a01.y) + (a23.x + a23.y));
     };
     // two accumulators: group g takes the units u = g, g + 2, .. (with two
-    // token pairs per tile, pair g of every tile in accumulator g; otherwise
-    // alternate tiles), every token of the unit; the accumulator goes back to
-    // the MMA before the unit's last logits are stored
-    for (int u = g; alt_units && u < n_comp * n_units && !s_abort; u += 2) {
-      const int i = u / n_units, pp = u - i * n_units, buf = u & 1, st = i % S;
-      if (!mbar_wait(&acc_full[buf], (u >> 1) & 1)) {
-        if (lane == 0) abort_now();
-        break;
-      }
-      tc_fence_after();
-      const int col = (t_begin + i) * kTileKeys + r;  // logits column of this lane's key
-      const int s = kb + col;
-      const float scale_k = ssc[st * kTileKeys + r];
-      const bool bad = s < seq_len && !block_ok(s);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[st]);  // this warp is done with the stage's scales
-      if (pair_split) {  // 64 heads: constant trip counts
-        const int j0 = 2 * pp, j1 = j0 + 1;
-        const float acc0 = head_sum(buf * acc_cols, j0, 0, 64);
-        const float acc1 = j1 < ntok ? head_sum(buf * acc_cols + 64, j1, 0, 64) : 0.f;
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[buf]);
-        if (col < p.ld) {
-          __stcs(p.logits + static_cast<int64_t>(s_tok[j0]) * p.ld + col,
-                 (s < s_valid[j0] && !bad) ? acc0 * scale_k : -INFINITY);
-          if (j1 < ntok)
-            __stcs(p.logits + static_cast<int64_t>(s_tok[j1]) * p.ld + col,
-                   (s < s_valid[j1] && !bad) ? acc1 * scale_k : -INFINITY);
+    // token pairs per tile, pair g of every tile; otherwise alternate tiles),
+    // always in accumulator g, every token of the unit; the accumulator goes
+    // back to the MMA before the unit's last logits are stored. The tokens of
+    // a group's units are the same in every tile, so their logits rows and
+    // causal limits are read once.
+    if (alt_units) {
+      const int di = n_units == 2 ? 1 : 2;  // tiles from one unit of the group to its next
+      const int j0 = n_units == 2 ? 2 * g : 0;
+      const int j_end = pair_split ? min(j0 + 2, ntok) : ntok;
+      float* row0 = p.logits + static_cast<int64_t>(s_tok[j0]) * p.ld;
+      float* row1 = p.logits + static_cast<int64_t>(s_tok[min(j0 + 1, ntok - 1)]) * p.ld;
+      const int valid0 = s_valid[j0], valid1 = s_valid[min(j0 + 1, ntok - 1)];
+      const uint32_t acc_col = g * acc_cols;
+      int i = n_units == 2 ? 0 : g;
+      int st = i % S;
+      for (int k = 0; i < n_comp && !s_abort; ++k) {
+        if (!mbar_wait(&acc_full[g], k & 1)) {
+          if (lane == 0) abort_now();
+          break;
         }
-        continue;
-      }
-      for (int j = 0; j < ntok; ++j) {
-        const float acc = head_sum(buf * acc_cols + j * p.hi_pad, j, 0, p.hi_pad);
-        if (j + 1 == ntok) {
+        tc_fence_after();
+        const int col = (t_begin + i) * kTileKeys + r;  // logits column of this lane's key
+        const int s = kb + col;
+        const float scale_k = ssc[st * kTileKeys + r];
+        const bool bad = s < seq_len && !block_ok(s);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[st]);  // this warp is done with the stage's scales
+        if (pair_split) {  // 64 heads: constant trip counts
+          const bool two = j0 + 1 < j_end;
+          const float acc0 = head_sum(acc_col, j0, 0, 64);
+          const float acc1 = two ? head_sum(acc_col + 64, j0 + 1, 0, 64) : 0.f;
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          if (lane == 0) mbar_arrive(&acc_empty[g]);
+          if (col < p.ld) {
+            __stcs(row0 + col, (s < valid0 && !bad) ? acc0 * scale_k : -INFINITY);
+            if (two) __stcs(row1 + col, (s < valid1 && !bad) ? acc1 * scale_k : -INFINITY);
+          }
+        } else {
+          for (int j = 0; j < ntok; ++j) {
+            const float acc = head_sum(acc_col + j * p.hi_pad, j, 0, p.hi_pad);
+            if (j + 1 == ntok) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acc_empty[g]);
+            }
+            if (col < p.ld)
+              __stcs(p.logits + static_cast<int64_t>(s_tok[j]) * p.ld + col,
+                     (s < s_valid[j] && !bad) ? acc * scale_k : -INFINITY);
+          }
         }
-        if (col < p.ld)
-          __stcs(p.logits + static_cast<int64_t>(s_tok[j]) * p.ld + col,
-                 (s < s_valid[j] && !bad) ? acc * scale_k : -INFINITY);
+        i += di;
+        st += di;
+        if (st >= S) st -= S;
       }
     }
     // one accumulator (more than 128 columns of fewer than 64 heads): both
