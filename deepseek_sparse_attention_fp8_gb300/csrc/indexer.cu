@@ -249,9 +249,9 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
     s_abort = 1;
     report(p.dev_status, DSA_DEVERR_TIMEOUT);
   };
+  auto block_id_ok = [&](int blk) { return blk >= 0 && blk < p.num_blocks; };
   auto block_ok = [&](int s) {  // key s < seq_len lies in a valid block
-    const int blk = s_blk[s / p.block_size - blk0];
-    return blk >= 0 && blk < p.num_blocks;
+    return block_id_ok(s_blk[s / p.block_size - blk0]);
   };
   // keys that later token blocks of the request read again stay in L2
   const bool keep_keys = p.n_tb > 1;
@@ -507,6 +507,11 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
       const uint32_t acc_col = g * acc_cols;
       int i = n_units == 2 ? 0 : g;
       int st = i % S;
+      // the block of this warp's 32 keys (one block: block_size is a multiple
+      // of 64), advanced with the tile instead of divided out per tile
+      const int key_w = kb + (t_begin + i) * kTileKeys + (warp & 3) * 32;
+      int blk_rel = key_w / p.block_size - blk0;
+      int blk_off = key_w - (blk_rel + blk0) * p.block_size;
       for (int k = 0; i < n_comp && !s_abort; ++k) {
         if (!mbar_wait(&acc_full[g], k & 1)) {
           if (lane == 0) abort_now();
@@ -516,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
         const int col = (t_begin + i) * kTileKeys + r;  // logits column of this lane's key
         const int s = kb + col;
         const float scale_k = ssc[st * kTileKeys + r];
-        const bool bad = s < seq_len && !block_ok(s);
+        const bool bad = s < seq_len && !block_id_ok(s_blk[blk_rel]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[st]);  // this warp is done with the stage's scales
         if (pair_split) {  // 64 heads: constant trip counts
@@ -546,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
         i += di;
         st += di;
         if (st >= S) st -= S;
+        for (blk_off += di * kTileKeys; blk_off >= p.block_size; blk_off -= p.block_size) ++blk_rel;
       }
     }
     // one accumulator (more than 128 columns of fewer than 64 heads): both
