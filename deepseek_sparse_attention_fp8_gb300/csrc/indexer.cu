@@ -476,18 +476,13 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
         a01 = __ffma2_rn(make_float2(w.x, w.y), make_float2(x0 + fabsf(x0), x1 + fabsf(x1)), a01);
         a23 = __ffma2_rn(make_float2(w.z, w.w), make_float2(x2 + fabsf(x2), x3 + fabsf(x3)), a23);
       };
-      for (int hc = h0; hc < h1; hc += 32) {
-        if (hc + 32 <= h1) {
-          uint32_t v[32];
-          tmem_ld32_sync(lane_addr + col + hc, v);
+      // 16 columns per tensor-memory load: measured faster than 32 (fewer
+      // registers held across the wait) and than 8 at every shape
+      for (int hc = h0; hc < h1; hc += 16) {
+        uint32_t v[16];
+        tmem_ld16_sync(lane_addr + col + hc, v);
 #pragma unroll
-          for (int x = 0; x < 8; ++x) step4(w4[hc / 4 + x], v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
-        } else {
-          uint32_t v[16];
-          tmem_ld16_sync(lane_addr + col + hc, v);
-#pragma unroll
-          for (int x = 0; x < 4; ++x) step4(w4[hc / 4 + x], v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
-        }
+        for (int x = 0; x < 4; ++x) step4(w4[hc / 4 + x], v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
       }
       return 0.5f * ((a01.x + a01.y) + (a23.x + a23.y));
     };
