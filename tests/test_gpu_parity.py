@@ -275,6 +275,38 @@ def test_bad_block_ids_are_masked_and_reported():
     assert np.all(np.isfinite(lg[0, :128]))
 
 
+@pytest.mark.parametrize("shape,bs", [("decode", 64), ("mtp2", 64), ("prefill", 64), ("prefill", 128),
+                                      ("prefill15", 128)])
+def test_bad_block_ids_are_masked_in_every_epilogue_shape(shape, bs):
+    """A bad block id in request 0's table masks exactly that block's keys to
+    -inf for every token of the request, whichever epilogue shape the CTA takes
+    (one token, two tokens, token pairs), and reports BLOCK_OOB; every other
+    logit is bit-identical to the run with the clean table."""
+    base, kw = HEAD_SHAPES[shape]
+    wl = make_workload(base, index_topk=256, block_size=bs, **kw)
+    step = DsaStep(wl)
+    step.indexer()
+    torch.cuda.synchronize()
+    clean = step.logits.cpu().numpy().copy()
+    bt = step.block_table.clone()
+    lb = 128 // bs  # the logical block holding key 128
+    bt[0, lb] = wl.num_blocks + 5
+    step.block_table.copy_(bt)
+    step.dev_status.zero_()
+    step.logits.fill_(float("nan"))
+    step.indexer()
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) & api.DSA_DEVERR_BLOCK_OOB
+    lg = step.logits.cpu().numpy()
+    k0, k1 = lb * bs, (lb + 1) * bs
+    rows0 = range(int(wl.query_start_loc[0]), int(wl.query_start_loc[1]))
+    for t in rows0:
+        assert np.all(np.isneginf(lg[t, k0:k1])), f"row {t}: bad block not masked"
+    keep = np.ones_like(lg, dtype=bool)
+    keep[list(rows0), k0:k1] = False
+    assert np.array_equal(lg[keep].view(np.uint32), clean[keep].view(np.uint32))
+
+
 def test_unused_block_table_entries_are_ignored():
     """Entries of a request's block-table row past its length may hold anything:
     the kernels may read them but never use them, so results are unchanged and
