@@ -104,7 +104,7 @@ struct MlaSmem {
   static constexpr int kXBuf = 128 * kXRow;
   static constexpr int kRow = kX + (C::kPair ? kXBufs * kXBuf : 0);
   static constexpr int kLive = kRow + kMaxSlots * 4;
-  static constexpr int kCoordStages = F8 ? kRStages : kBStages;
+  static constexpr int kCoordStages = F8 ? kRStages : 0;  // gather rows of the fp8 producer's raw stages
   static constexpr int kCoord = kLive + kBStages * 4 * 2;
   static constexpr int kRed = kCoord + kCoordStages * kTileKeys * 4;
   static constexpr int kTotal = kRed + 6 * 128 * 4 + 1024;
@@ -497,8 +497,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     const int pw = warp - kProdWarp0;
     const uint32_t tile_bytes = kTileKeys * (nkb * 128 + (C::kRopeHalf ? 64 : 0));
     int issued = 0;
+    // row of key pw * 16 + lane of the next tile (lanes 0-15), read before
+    // the wait for its stage
+    auto tile_row = [&](int i) {
+      const int sl = i * kTileKeys + pw * 16 + lane;
+      return (lane < 16 && sl < n_slots) ? row_sm[sl] : -1;
+    };
+    int row_next = n_tiles > 0 ? tile_row(0) : -1;
     for (int i = 0; i < n_tiles && !s_abort; ++i) {
       const int st = i % kBS;
+      const int row = row_next;
+      if (i + 1 < n_tiles) row_next = tile_row(i + 1);
       if (i >= kBS && !mbar_wait(&kv_empty[st], ((i / kBS) - 1) & 1)) {
         if (lane == 0) abort_now();
         break;
@@ -507,31 +516,26 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
         if (lane == 0) abort_now();
         break;
       }
-      bool live = false;
-      if (lane < 16) {
-        const int kr = pw * 16 + lane;
-        const int sl = i * kTileKeys + kr;
-        const int row = sl < n_slots ? row_sm[sl] : -1;
-        live = row >= 0;
-        coord_sm[st * kTileKeys + kr] = live ? row : p.total_rows;  // out of range: zero fill
-      }
+      const bool live = row >= 0;
+      const int crd = live ? row : p.total_rows;  // out of range: zero fill
       const uint32_t mask = __ballot_sync(0xFFFFFFFFu, live);
       if (lane == 0) live_m[st * 4 + pw] = static_cast<uint16_t>(mask);
-      __syncwarp();
+      // the 4 rows of gather group lane % 4 of this warp
+      const int gs = 4 * (lane & 3);
+      const int c0 = __shfl_sync(0xFFFFFFFFu, crd, gs), c1 = __shfl_sync(0xFFFFFFFFu, crd, gs + 1),
+                c2 = __shfl_sync(0xFFFFFFFFu, crd, gs + 2), c3 = __shfl_sync(0xFFFFFFFFu, crd, gs + 3);
       if (lane == 0) {
         if (pw == 0) mbar_arrive_expect_tx(&kv_full[st], tile_bytes);
         else mbar_arrive(&kv_full[st]);
       }
       if (lane < 4 * nkb) {
         const int g = pw * 4 + (lane & 3), kb = lane >> 2;
-        const int* cs = coord_sm + st * kTileKeys + 4 * g;
         tma_gather4(smem_u32(kv_sm + st * L::kKvStage + kb * L::kKvKb + g * 512), &kvmap, &kv_full[st],
-                    (kb0 + kb) * 64, cs[0], cs[1], cs[2], cs[3]);
+                    (kb0 + kb) * 64, c0, c1, c2, c3);
       } else if (C::kRopeHalf && lane < 4 * nkb + 4) {  // the rope half of the same 4-row groups
         const int g = pw * 4 + (lane & 3);
-        const int* cs = coord_sm + st * kTileKeys + 4 * g;
-        tma_gather4(smem_u32(kv_sm + st * L::kKvStage + L::kKvHalf + g * 256), &kvmap64, &kv_full[st], rope_kv, cs[0],
-                    cs[1], cs[2], cs[3]);
+        tma_gather4(smem_u32(kv_sm + st * L::kKvStage + L::kKvHalf + g * 256), &kvmap64, &kv_full[st], rope_kv, c0,
+                    c1, c2, c3);
       }
       issued = i + 1;
     }
