@@ -255,41 +255,43 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   };
   // keys that later token blocks of the request read again stay in L2
   const bool keep_keys = p.n_tb > 1;
-  // tile i: two TMA loads of 64 keys x 128 B (one page each) plus their scales,
-  // completing on full_bar[i % S]; keys past seq_len are neither loaded nor counted
-  auto issue_keys = [&](int i) {
-    const int st = i % S;
-    const int key0 = kb + (t_begin + i) * kTileKeys;
-    uint32_t bytes = 0;
-    int blk_u[2], off_u[2];
+  // tile i: two TMA loads of 64 keys x 128 B (one page each) plus their
+  // scales, completing on full_bar[st]; keys past seq_len are neither loaded
+  // nor counted. Issued by lanes 0 and 1 of the producer warp together, lane u
+  // the half of keys 64u.. (one instruction issues both halves' copies), for
+  // tiles in order: each lane's block and offset in it advance with the tile
+  // (block_size is a multiple of 64) instead of being divided out per tile.
+  int iss_blk = 0, iss_off = 0;
+  {
+    const int s0 = kb + t_begin * kTileKeys + 64 * (lane & 1);
+    iss_blk = s0 / p.block_size - blk0;
+    iss_off = s0 - (iss_blk + blk0) * p.block_size;
+  }
+  auto issue_keys = [&](int i, int st) {
+    const int s0 = kb + (t_begin + i) * kTileKeys + 64 * lane;
+    int blk = -1;
     bool bad = false;
-    for (int u = 0; u < 2; ++u) {
-      const int s0 = key0 + 64 * u;
-      blk_u[u] = -1;
-      off_u[u] = s0 % p.block_size;
-      if (s0 < seq_len) {
-        if (block_ok(s0)) {
-          blk_u[u] = s_blk[s0 / p.block_size - blk0];
-          bytes += 64 * 128 + 64 * 4;
-        } else {
-          bad = true;
-        }
-      }
+    if (s0 < seq_len) {
+      const int b = s_blk[iss_blk];
+      if (block_id_ok(b)) blk = b;
+      else bad = true;
     }
-    mbar_arrive_expect_tx(&full_bar[st], bytes);
-    for (int u = 0; u < 2; ++u) {
-      if (blk_u[u] < 0) continue;
+    const uint32_t halves = __ballot_sync(0x3u, blk >= 0);
+    if (lane == 0) mbar_arrive_expect_tx(&full_bar[st], __popc(halves) * (64 * 128 + 64 * 4));
+    __syncwarp(0x3u);
+    if (blk >= 0) {
       if (keep_keys)
-        tma_load_3d_hint(smem_u32(sk + st * kTileBytes + u * 8192), &kmap, &full_bar[st], 0, off_u[u], blk_u[u],
+        tma_load_3d_hint(smem_u32(sk + st * kTileBytes + lane * 8192), &kmap, &full_bar[st], 0, iss_off, blk,
                          l2_policy_evict_last());
       else
-        tma_load_3d(smem_u32(sk + st * kTileBytes + u * 8192), &kmap, &full_bar[st], 0, off_u[u], blk_u[u]);
-      bulk_copy_g2s(smem_u32(ssc + st * kTileKeys + u * 64),
-                    p.k_cache + static_cast<int64_t>(blk_u[u]) * p.k_block_stride +
-                        static_cast<int64_t>(p.block_size) * 128 + off_u[u] * 4,
+        tma_load_3d(smem_u32(sk + st * kTileBytes + lane * 8192), &kmap, &full_bar[st], 0, iss_off, blk);
+      bulk_copy_g2s(smem_u32(ssc + st * kTileKeys + lane * 64),
+                    p.k_cache + static_cast<int64_t>(blk) * p.k_block_stride +
+                        static_cast<int64_t>(p.block_size) * 128 + iss_off * 4,
                     256, &full_bar[st]);
     }
     if (bad) report(p.dev_status, DSA_DEVERR_BLOCK_OOB);
+    for (iss_off += kTileKeys; iss_off >= p.block_size; iss_off -= p.block_size) ++iss_blk;
   };
   // tiles whose loads the producer issues before the CTA barrier (TMA path):
   // one, so that its latency overlaps the prologue; issuing every stage this
@@ -356,11 +358,14 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
         }
         mbar_init(&q_ready, 8);
         fence_mbar_init();
-        // the tile's block ids were stored by this warp (its first 32 entries
-        // cover the first 16 tiles: block_size >= 64)
-        if constexpr (DI == 128) {
-          for (int i = 0; i < n_early; ++i) issue_keys(i);
-        }
+      }
+      // the tiles' block ids were stored by this warp (its first 32 entries
+      // cover the first 16 tiles: block_size >= 64), the barriers initialised
+      // by its lane 0
+      if constexpr (DI == 128) {
+        __syncwarp();
+        if (warp == kProdWarp && lane < 2)
+          for (int i = 0; i < n_early; ++i) issue_keys(i, i);
       }
       if (warp == kMmaWarp) {
         tmem_alloc(&tmem_holder, tmem_cols);
@@ -381,15 +386,16 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
 
   if (n_comp > 0 && warp == kProdWarp) {
     // ---------------- producer (the first tile went out before the CTA barrier)
+    // stage of tile i and how many times the ring has wrapped before it
+    int st = n_early, wraps = 0;
     for (int i = n_early; i < n_comp && !s_abort; ++i) {
-      const int st = i % S;
-      if (i >= S && !mbar_wait(&empty_bar[st], ((i / S) - 1) & 1)) {
+      if (i >= S && !mbar_wait(&empty_bar[st], (wraps - 1) & 1)) {
         if (lane == 0) abort_now();
         break;
       }
       const int key0 = kb + (t_begin + i) * kTileKeys;
       if constexpr (DI == 128) {
-        if (lane == 0) issue_keys(i);
+        if (lane < 2) issue_keys(i, st);
       } else {
         constexpr int kChunks = DI / 16;
         uint8_t* dst_base = sk + st * kTileBytes;
@@ -422,17 +428,22 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
         }
         cp_async_mbar_arrive(&full_bar[st]);
       }
+      if (++st == S) {
+        st = 0;
+        ++wraps;
+      }
     }
   } else if (n_comp > 0 && warp == kMmaWarp) {
     // ---------------- MMA issuer
     const uint32_t idesc = idesc_e4m3(128, unit_cols);
     if (!mbar_wait(&q_ready, 0) && lane == 0) abort_now();
+    int st = 0, wraps = 0;  // stage of tile i and how many times the ring has wrapped before it
     for (int i = 0; i < n_comp && !s_abort; ++i) {
-      const int st = i % S;
-      bool ok = mbar_wait(&full_bar[st], (i / S) & 1);
+      bool ok = mbar_wait(&full_bar[st], wraps & 1);
       for (int pp = 0; ok && pp < n_units; ++pp) {
-        const int u = i * n_units + pp, buf = u % nbuf;
-        if (u >= nbuf) ok = mbar_wait(&acc_empty[buf], ((u / nbuf) - 1) & 1);
+        const int u = i * n_units + pp;
+        const int buf = nbuf == 2 ? u & 1 : 0, use = nbuf == 2 ? u >> 1 : u;  // accumulator, its use count
+        if (u >= nbuf) ok = mbar_wait(&acc_empty[buf], (use - 1) & 1);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -450,6 +461,10 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
       if (!ok) {
         if (lane == 0) abort_now();
         break;
+      }
+      if (++st == S) {
+        st = 0;
+        ++wraps;
       }
     }
   } else if (n_comp > 0) {
