@@ -134,6 +134,7 @@ struct IndexerParams {
   int64_t key_begin;  // key of logits column 0 (a window of the keys; a multiple of 128 and of block_size)
   int64_t key_cap;    // requests are clipped to keys below this (ld for the whole-row call)
   int32_t* dev_status;
+  int32_t lpt;  // hand out the (row, chunk) pairs longest work first (rows <= kThreads)
 };
 
 struct SmemOffsets {
@@ -169,10 +170,82 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // the top-k kernel may be scheduled now; it waits for this grid's results
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int b = blockIdx.y / p.n_tb;
-  const int tblk = blockIdx.y % p.n_tb;
+  // the CTA's row (request b, token block tblk) and chunk of tiles
+  int b, tblk, chunk;
+  if (p.lpt) {
+    // Longest work first: the grid's (row, chunk) pairs, in the order the
+    // block scheduler starts CTAs, are every row's full chunks, then each
+    // row's partial last chunk, then the chunks past its last key (which only
+    // write -inf), so that with requests of different lengths the long rows'
+    // chunks start early and the last CTAs to start are short ones. The order
+    // only permutes the pairs; each CTA derives its bounds below as before.
+    // Thread i < rows counts row i's chunks (rows * gridDim.x < 2^21).
+    __shared__ uint64_t s_wsum[kThreads / 32];
+    __shared__ int s_row, s_chunk;
+    const int R = p.B * p.n_tb, nx = static_cast<int>(gridDim.x), tpc = p.tiles_per_cta;
+    int full = 0, part = 0, empty = 0;
+    if (tid < R) {
+      const int bi = tid / p.n_tb, ti = tid - bi * p.n_tb;
+      const int q0i = __ldg(p.qsl + bi), q1i = __ldg(p.qsl + bi + 1), tok0i = q0i + ti * p.tb;
+      int tiles = 0;
+      if (tok0i < q1i) {
+        const int last = min(tok0i + p.tb, q1i) - 1;  // the block's last token
+        const int64_t vmax = static_cast<int64_t>(__ldg(p.seq_lens + bi)) - (q1i - q0i) + (last - q0i) + 1;
+        const int64_t v = min(vmax, p.key_cap) - p.key_begin;
+        tiles = static_cast<int>(max(static_cast<int64_t>(0), min((v + kTileKeys - 1) / kTileKeys,
+                                                                  static_cast<int64_t>(p.n_tiles))));
+      }
+      full = min(tiles / tpc, nx);
+      part = (full < nx && tiles % tpc != 0) ? 1 : 0;
+      empty = nx - full - part;
+    }
+    constexpr uint64_t kM = (1u << 21) - 1;
+    const uint64_t v = static_cast<uint64_t>(full) | (static_cast<uint64_t>(part) << 21) |
+                       (static_cast<uint64_t>(empty) << 42);
+    uint64_t x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) s_wsum[warp] = x;
+    __syncthreads();
+    uint64_t before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const uint64_t ws = s_wsum[w];
+      if (w < warp) before += ws;
+      total += ws;
+    }
+    const uint64_t ex = before + x - v;
+    const int fi = static_cast<int>(ex & kM), pi = static_cast<int>((ex >> 21) & kM), ei = static_cast<int>(ex >> 42);
+    const int F = static_cast<int>(total & kM), P = static_cast<int>((total >> 21) & kM);
+    const int L = static_cast<int>(blockIdx.y) * nx + static_cast<int>(blockIdx.x);
+    if (tid < R) {
+      int c = -1;
+      if (L < F) {
+        if (L >= fi && L < fi + full) c = L - fi;
+      } else if (L < F + P) {
+        if (part && L - F == pi) c = full;
+      } else if (L - F - P >= ei && L - F - P < ei + empty) {
+        c = full + part + (L - F - P - ei);
+      }
+      if (c >= 0) {
+        s_row = tid;
+        s_chunk = c;
+      }
+    }
+    __syncthreads();
+    b = s_row / p.n_tb;
+    tblk = s_row - b * p.n_tb;
+    chunk = s_chunk;
+  } else {
+    b = blockIdx.y / p.n_tb;
+    tblk = blockIdx.y % p.n_tb;
+    chunk = blockIdx.x;
+  }
   // tiles are counted in logits columns; tile i holds keys key_begin + 128 i ..
-  const int t_begin = blockIdx.x * p.tiles_per_cta;
+  const int t_begin = chunk * p.tiles_per_cta;
   const int t_end = min(t_begin + p.tiles_per_cta, p.n_tiles);
   const int kb = static_cast<int>(p.key_begin);
   // block ids of every key the CTA's tiles can address (warps 8 and 9), read
@@ -199,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   // clip the request to what the logits row and the block table can address
   const int64_t cap = min(p.key_cap, static_cast<int64_t>(p.bt_stride) * p.block_size);
   if (seq_len < q_len || seq_len > cap) {
-    if (tid == 0 && blockIdx.x == 0) report(p.dev_status, DSA_DEVERR_SEQ_LEN);
+    if (tid == 0 && chunk == 0) report(p.dev_status, DSA_DEVERR_SEQ_LEN);
     seq_len = max(q_len, static_cast<int>(min(static_cast<int64_t>(seq_len), cap)));
   }
   const int max_valid = min(static_cast<int64_t>(seq_len - q_len + (tok0 + ntok - 1 - q0) + 1), cap);
@@ -683,12 +756,27 @@ dsa_status_t indexer_launch(const IndexerCall& c, float* logits, int64_t ld, int
   const int64_t rows = static_cast<int64_t>(c.B) * p.n_tb;
   if (rows > 65535) return fail(DSA_ERR_UNSUPPORTED, "indexer: B * token blocks = %lld > 65535", (long long)rows);
   if (key_begin + ld > 0x7FFFFFFF) return fail(DSA_ERR_UNSUPPORTED, "indexer: key positions beyond int32");
-  // one wave of two CTAs per SM when the work allows it, at least two tiles per CTA
   const int64_t slots = 2LL * num_sms();
   const int64_t total_tiles = rows * p.n_tiles;
-  int64_t tpc = std::max<int64_t>(2, (total_tiles + slots - 1) / slots);
-  while (tpc < kMaxTilesPerCta && rows * ((p.n_tiles + tpc - 1) / tpc) > slots) ++tpc;
+  // Several tokens per request and few rows (batches of short multi-token
+  // steps, whose requests' lengths differ and are on the device only): chunks
+  // of about 1 / 2.5 of an even share of the rows' key ranges, handed out
+  // longest work first, so that chunks of the long requests start early and
+  // the ones past the short requests' keys cost a launch each. Otherwise one
+  // wave of two CTAs per SM when the work allows it, at least two tiles per
+  // CTA (the ordering's extra round trip for every row's length costs a
+  // decode batch more than it saves on even lengths: measured).
+  const bool lpt = c.max_q_len >= 2 && rows <= kThreads;
+  int64_t tpc;
+  if (lpt) {
+    tpc = std::max<int64_t>(4, (2 * total_tiles + 5 * slots - 1) / (5 * slots));
+  } else {
+    tpc = std::max<int64_t>(2, (total_tiles + slots - 1) / slots);
+    while (tpc < kMaxTilesPerCta && rows * ((p.n_tiles + tpc - 1) / tpc) > slots) ++tpc;
+  }
   p.tiles_per_cta = static_cast<int32_t>(std::min<int64_t>(tpc, kMaxTilesPerCta));
+  const int64_t grid_x = (p.n_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta;
+  p.lpt = lpt && rows * grid_x < (int64_t{1} << 21) ? 1 : 0;
   const int n_cols = p.hi_pad * p.tb;
   p.stages = indexer_stages(n_cols);
   const SmemOffsets so = indexer_smem(n_cols, p.stages);
