@@ -9,13 +9,16 @@
 // indexer q). Keys outside the causal range get -inf and every entry of a
 // row up to ld is written (the PR's clean_logits contract).
 //
-// One tcgen05 e4m3 MMA per 128-key tile: A = the key tile (M = 128 keys,
+// tcgen05 e4m3 MMAs per 128-key tile: A = the key tile (M = 128 keys,
 // K = head_dim bytes, 128-byte swizzled), B = the quantised queries of up to
-// four tokens of one request (N = 64 heads x tokens). Each TMEM lane then holds
-// one key, so the ReLU-weighted head sum is an in-thread loop over columns.
-// Key tiles come through the block table into a ring of shared-memory stages
-// (TMA page loads for 128-dim keys, 16-byte cp.async otherwise); two CTAs
-// share an SM so one CTA's epilogue overlaps the other's loads and MMAs.
+// four tokens of one request (N = 64 heads x tokens, or one MMA per token
+// pair with four tokens of 64 heads). Each TMEM lane then holds one key, so
+// the ReLU-weighted head sum is an in-thread loop over columns; two
+// accumulators let one epilogue warp group sum one unit while the other
+// unit's MMA runs. Key tiles come through the block table into a ring of
+// shared-memory stages (TMA page loads for 128-dim keys, 16-byte cp.async
+// otherwise); two CTAs share an SM so one CTA's epilogue overlaps the other's
+// loads and MMAs.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -154,7 +157,8 @@ __host__ __device__ inline int indexer_stages(int n_cols) { return n_cols <= 64 
 
 // Warp roles: warps 0-7 quantise the queries, then run the epilogue (warps w
 // and w + 4 read TMEM lanes 32(w%4)..+31 = keys of the tile); warp 8 loads key
-// tiles (TMA for 128-byte rows, cp.async otherwise); warp 9 issues the MMAs.
+// tiles (TMA for 128-byte rows from lanes 0 and 1, cp.async otherwise); warp 9
+// issues the MMAs.
 template <int DI>
 __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __grid_constant__ IndexerParams p,
                                                                      const __grid_constant__ CUtensorMap kmap) {
