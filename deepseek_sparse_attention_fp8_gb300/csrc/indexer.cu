@@ -154,6 +154,13 @@ __host__ __device__ inline SmemOffsets indexer_smem(int n_cols, int stages) {
 }
 // two CTAs per SM: stages sized so that 2 x smem stays within 228 KB
 __host__ __device__ inline int indexer_stages(int n_cols) { return n_cols <= 64 ? 6 : (n_cols <= 128 ? 5 : 4); }
+// three or four tokens of 64 heads: one MMA per token pair (see the kernel)
+__host__ __device__ inline bool indexer_pair_split(int hi_pad, int tb) { return hi_pad == 64 && tb > 2; }
+// query rows staged as the MMA's B operand: every pair's rows, so that with
+// an odd token count the last pair's MMA reads zero rows, not past the region
+__host__ __device__ inline int indexer_q_rows(int hi_pad, int tb) {
+  return indexer_pair_split(hi_pad, tb) ? 2 * ((tb + 1) / 2) * hi_pad : hi_pad * tb;
+}
 
 // Warp roles: warps 0-7 quantise the queries, then run the epilogue (warps w
 // and w + 4 read TMEM lanes 32(w%4)..+31 = keys of the tile); warp 8 loads key
@@ -283,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
 
   const int t_comp_end = min(t_end, (max_valid - kb + kTileKeys - 1) / kTileKeys);  // tiles needing an MMA
   const int n_comp = max(0, t_comp_end - t_begin);
-  const int n_cols = p.hi_pad * p.tb;  // MMA N
+  const int n_cols = indexer_q_rows(p.hi_pad, p.tb);  // staged query rows (the MMA N without pairs)
   const int S = p.stages;
   // MMA units: a unit is one MMA of a key tile against unit_cols query
   // columns into one of nbuf accumulators. When all the CTA's columns fit
@@ -291,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 2) indexer_logits_kernel(const __gri
   // three or four tokens of 64 heads they fit once, so a unit is one pair of
   // tokens: the key tile stays for both pairs and one pair's epilogue overlaps
   // the next pair's MMA, which a single 256-column accumulator would serialise.
-  const bool pair_split = p.hi_pad == 64 && p.tb > 2;
+  const bool pair_split = indexer_pair_split(p.hi_pad, p.tb);
   const int n_units = pair_split ? (ntok + 1) / 2 : 1;  // MMA units per key tile
   const int unit_cols = pair_split ? 2 * p.hi_pad : n_cols;
   const int nbuf = 2 * unit_cols <= 256 ? 2 : 1;
@@ -781,7 +788,7 @@ dsa_status_t indexer_launch(const IndexerCall& c, float* logits, int64_t ld, int
   p.tiles_per_cta = static_cast<int32_t>(std::min<int64_t>(tpc, kMaxTilesPerCta));
   const int64_t grid_x = (p.n_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta;
   p.lpt = lpt && rows * grid_x < (int64_t{1} << 21) ? 1 : 0;
-  const int n_cols = p.hi_pad * p.tb;
+  const int n_cols = indexer_q_rows(p.hi_pad, p.tb);
   p.stages = indexer_stages(n_cols);
   const SmemOffsets so = indexer_smem(n_cols, p.stages);
   const int max_smem = std::max(indexer_smem(64, indexer_stages(64)).total,
