@@ -101,9 +101,11 @@ def _e4m3_codes(x: np.ndarray) -> np.ndarray:
 
 def make_workload(name: str, seed: int | None = None, *, B: int | None = None, L=None, q_len: int | None = None,
                   index_topk: int | None = None, ld_pad: int = 128, lens=None, block_size: int = 64,
-                  q_std: float = 1.0, kv_fp8: bool = False, Hi: int | None = None, Di: int | None = None) -> Workload:
+                  q_std: float = 1.0, kv_fp8: bool = False, Hi: int | None = None, Di: int | None = None,
+                  q_lens=None) -> Workload:
     """Build one of the named workloads (optionally overriding a few sizes
-    for smaller parity cases). `lens` gives explicit per-request lengths;
+    for smaller parity cases). `lens` gives explicit per-request lengths and
+    `q_lens` per-request query counts (with `lens`, one entry per request);
     `q_std` the standard deviation of the MLA queries (1 in every workload);
     `kv_fp8` also lays the latent rows out as an fp8 latent cache; `Hi` and
     `Di` change the indexer's head count and head dim."""
@@ -139,7 +141,12 @@ def make_workload(name: str, seed: int | None = None, *, B: int | None = None, L
         seq_lens = np.full(Bn, spec["L"], dtype=np.int32)
     seq_lens = np.maximum(seq_lens, qn).astype(np.int32)
 
-    q_lens = np.full(Bn, qn, dtype=np.int32)
+    if q_lens is not None:
+        q_lens = np.asarray(q_lens, dtype=np.int32)
+        assert len(q_lens) == Bn and np.all(q_lens >= 1)
+        seq_lens = np.maximum(seq_lens, q_lens).astype(np.int32)
+    else:
+        q_lens = np.full(Bn, qn, dtype=np.int32)
     qsl = np.zeros(Bn + 1, dtype=np.int32)
     qsl[1:] = np.cumsum(q_lens)
     T = int(qsl[-1])

@@ -19,6 +19,12 @@ LOGIT_FLOOR = 1e-2
 ATT_MAX_ABS = 2e-2
 ATT_MEAN_ABS = 2e-3
 ATT_RMS_REL = 1e-2
+# lse: the kernel's softmax normaliser sums the bf16-rounded weights that its
+# PV product uses, each within a relative 2^-9 of the exact weight, so ln l
+# may be off by up to ln(1 + 2^-9) = 1.95e-3 (reached when a row has a few
+# dominant keys); beyond |lse| = 2.5 the bound is 1e-3 relative.
+LSE_ABS = 2.5e-3
+LSE_REL = 1e-3
 
 
 def oracle_q_quant(wl):
@@ -86,5 +92,7 @@ def check_attention(got, ref, rows, got_lse=None, ref_lse=None):
         gl, rl = got_lse[rows].astype(np.float64), ref_lse[rows]
         fin = np.isfinite(rl)
         assert np.array_equal(np.isfinite(gl), fin)
-        assert np.all(np.abs(gl[fin] - rl[fin]) <= 1e-3 * np.maximum(1.0, np.abs(rl[fin])))
+        bound = np.maximum(LSE_ABS, LSE_REL * np.abs(rl[fin]))
+        assert np.all(np.abs(gl[fin] - rl[fin]) <= bound), \
+            f"lse error {np.max(np.abs(gl[fin] - rl[fin]) - bound):.3g} over the bound"
     return float(err.max()), float(err.mean()), rms_rel

@@ -123,6 +123,36 @@ def test_indexer_logits_head_shapes(shape, Hi, Di):
     check_topk_sets(idx, O.topk(got, wl.seq_lens, wl.query_start_loc, wl.index_topk), range(wl.T))
 
 
+RAGGED_STEPS = {
+    # requests of one to three query tokens and very different lengths (one
+    # token block each): chunks of the longest-work-first order of every kind
+    "q3": dict(lens=[50, 5000, 700, 12000, 3, 2048], q_lens=[1, 3, 2, 3, 1, 2]),
+    # up to six tokens (token blocks of four): second blocks of one or two
+    # tokens, and rows with no second block
+    "q6": dict(lens=[6, 9000, 130, 4100, 2500], q_lens=[6, 5, 1, 4, 2]),
+}
+
+
+@pytest.mark.parametrize("case", sorted(RAGGED_STEPS))
+def test_ragged_multi_token_batch(case):
+    """A batch of requests with different query counts and lengths (the
+    indexer hands out its work longest first there): every logit against the
+    oracle on a dirty buffer, the top-k of the same logits exact, and the
+    attention against the oracle."""
+    wl = make_workload("mixed_b64_mtp2", index_topk=512, **RAGGED_STEPS[case])
+    step = DsaStep(wl)
+    step.logits.fill_(float("nan"))
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) == 0
+    got = step.logits.cpu().numpy()
+    check_logits(got, oracle_logits(wl), range(wl.T))
+    idx = step.topk_idx.cpu().numpy()
+    check_topk_sets(idx, O.topk(got, wl.seq_lens, wl.query_start_loc, wl.index_topk), range(wl.T))
+    ref, ref_lse = oracle_attention(wl, idx)
+    check_attention(step.out.float().cpu().numpy(), ref, np.arange(wl.T), step.lse.cpu().numpy(), ref_lse)
+
+
 def test_topk_exact_on_same_logits(run_small):
     wl, step = run_small
     logits = step.logits.cpu().numpy()
