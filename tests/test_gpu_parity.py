@@ -92,6 +92,7 @@ def test_indexer_logits(run_small):
 HEAD_SHAPES = {
     "decode": ("decode_b32_l8192", dict(lens=[700, 1500, 333])),
     "mtp2": ("mixed_b64_mtp2", dict(lens=[900, 1300, 65])),
+    "mtp3": ("mixed_b64_mtp2", dict(lens=[900, 1300, 65], q_len=3)),
     "prefill": ("prefill_4096_of_65536", dict(L=900, q_len=13)),
     "prefill14": ("prefill_4096_of_65536", dict(L=900, q_len=14)),
     "prefill15": ("prefill_4096_of_65536", dict(L=900, q_len=15)),
@@ -103,7 +104,7 @@ HEAD_SHAPES = {
 def test_indexer_logits_head_shapes(shape, Hi, Di):
     """The logits kernel over indexer head counts (padded to multiples of 16)
     and head dims 32, 64 and 128 (TMA key pages for 128, 16-byte copies
-    otherwise), for one, two and four tokens per CTA: two accumulators taken
+    otherwise), for one, two, three and four tokens per CTA: two accumulators taken
     by the two epilogue warp groups in turn (whole tiles, or token pairs for
     three or four tokens of 64 heads), or one accumulator read by both groups
     when fewer than 64 heads of four tokens fill more than 128 columns; the
