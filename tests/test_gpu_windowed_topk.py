@@ -24,6 +24,8 @@ CASES = {
     "decode_topk256": ("decode_b32_l8192", dict(lens=[300, 129, 64, 4000, 2600], index_topk=256)),
     "mtp2_small": ("mixed_b64_mtp2", dict(lens=[1500, 2049, 3000, 65], index_topk=2048)),
     "prefill_small": ("prefill_4096_of_65536", dict(L=2300, q_len=260, index_topk=512)),
+    "ragged_q3": ("mixed_b64_mtp2", dict(lens=[50, 5000, 700, 12000, 3, 2048], q_lens=[1, 3, 2, 3, 1, 2],
+                                         index_topk=512)),
 }
 
 
