@@ -134,6 +134,27 @@ RAGGED_STEPS = {
 }
 
 
+@pytest.mark.parametrize("bs", [192, 256])
+@pytest.mark.parametrize("base,kw", [("decode_b32_l8192", dict(lens=[3000, 1111, 200])),
+                                     ("mixed_b64_mtp2", dict(lens=[900, 5000, 65], q_lens=[3, 2, 1]))],
+                         ids=["decode", "ragged"])
+def test_other_block_sizes(base, kw, bs):
+    """Block sizes other than 64 and 128 (any multiple of 64 is accepted):
+    the whole step against the oracle."""
+    wl = make_workload(base, index_topk=512, block_size=bs, **kw)
+    step = DsaStep(wl)
+    step.logits.fill_(float("nan"))
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) == 0
+    got = step.logits.cpu().numpy()
+    check_logits(got, oracle_logits(wl), range(wl.T))
+    idx = step.topk_idx.cpu().numpy()
+    check_topk_sets(idx, O.topk(got, wl.seq_lens, wl.query_start_loc, wl.index_topk), range(wl.T))
+    ref, ref_lse = oracle_attention(wl, idx)
+    check_attention(step.out.float().cpu().numpy(), ref, np.arange(wl.T), step.lse.cpu().numpy(), ref_lse)
+
+
 @pytest.mark.parametrize("case", sorted(RAGGED_STEPS))
 def test_ragged_multi_token_batch(case):
     """A batch of requests with different query counts and lengths (the
