@@ -155,6 +155,28 @@ def test_other_block_sizes(base, kw, bs):
     check_attention(step.out.float().cpu().numpy(), ref, np.arange(wl.T), step.lse.cpu().numpy(), ref_lse)
 
 
+def test_many_requests():
+    """1100 short requests (more than any kernel's threads per CTA, so the
+    request lookups take their loop paths): the whole step against the oracle
+    on sampled rows, every logit checked."""
+    rng = np.random.default_rng(11)
+    lens = rng.integers(64, 700, 1100)
+    wl = make_workload("decode_b32_l8192", index_topk=64, lens=lens.tolist())
+    step = DsaStep(wl)
+    step.logits.fill_(float("nan"))
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) == 0
+    rows = sorted(set(rng.integers(0, wl.T, 48).tolist()) | {0, wl.T - 1})
+    got = step.logits.cpu().numpy()
+    assert not np.isnan(got).any(), "logits left unwritten"
+    check_logits(got, oracle_logits(wl, rows=rows), rows)
+    idx = step.topk_idx.cpu().numpy()
+    check_topk_sets(idx, O.topk(got, wl.seq_lens, wl.query_start_loc, wl.index_topk, rows=rows), rows)
+    ref, ref_lse = oracle_attention(wl, idx, rows=rows)
+    check_attention(step.out.float().cpu().numpy(), ref, np.array(rows), step.lse.cpu().numpy(), ref_lse)
+
+
 @pytest.mark.parametrize("case", sorted(RAGGED_STEPS))
 def test_ragged_multi_token_batch(case):
     """A batch of requests with different query counts and lengths (the
