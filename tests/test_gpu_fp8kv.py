@@ -21,6 +21,9 @@ CASES = {
     "mtp2_small": ("mixed_b64_mtp2", dict(lens=[1500, 2049, 3000, 65], index_topk=2048)),
     "prefill_small": ("prefill_4096_of_65536", dict(L=2300, q_len=260, index_topk=512)),
     "decode_topk_small": ("decode_b32_l8192", dict(lens=[300, 129, 64, 4000], index_topk=256)),
+    "ragged_q3": ("mixed_b64_mtp2", dict(lens=[50, 5000, 700, 12000, 3, 2048], q_lens=[1, 3, 2, 3, 1, 2],
+                                         index_topk=512)),
+    "bs192": ("decode_b32_l8192", dict(lens=[3000, 1111, 200], index_topk=512, block_size=192)),
 }
 
 
