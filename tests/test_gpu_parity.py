@@ -155,9 +155,32 @@ def test_other_block_sizes(base, kw, bs):
     check_attention(step.out.float().cpu().numpy(), ref, np.arange(wl.T), step.lse.cpu().numpy(), ref_lse)
 
 
-def test_many_requests():
+@pytest.mark.parametrize("K", [100, 2047])
+def test_unpadded_logits_rows_and_odd_topk(K):
+    """Logits rows exactly as long as the longest request (ld = 2999, not a
+    multiple of the 128-key tile nor of 16 bytes) and an index_topk that is
+    not a multiple of the 64-key attention tile: the whole step against the
+    oracle, every logit written."""
+    wl = make_workload("decode_b32_l8192", index_topk=K, lens=[2999, 1001, 77, 2100], ld_pad=1)
+    assert wl.ld == 2999
+    step = DsaStep(wl)
+    step.logits.fill_(float("nan"))
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) == 0
+    got = step.logits.cpu().numpy()
+    assert not np.isnan(got).any(), "logits left unwritten"
+    check_logits(got, oracle_logits(wl), range(wl.T))
+    idx = step.topk_idx.cpu().numpy()
+    check_topk_sets(idx, O.topk(got, wl.seq_lens, wl.query_start_loc, wl.index_topk), range(wl.T))
+    ref, ref_lse = oracle_attention(wl, idx)
+    check_attention(step.out.float().cpu().numpy(), ref, np.arange(wl.T), step.lse.cpu().numpy(), ref_lse)
+
+
+def test_more_requests_than_any_cta_has_threads():
     """1100 short requests (more than any kernel's threads per CTA, so the
-    request lookups take their loop paths): the whole step against the oracle
+    request lookups take their loop paths, the top-k's included): the whole
+    step against the oracle
     on sampled rows, every logit checked."""
     rng = np.random.default_rng(11)
     lens = rng.integers(64, 700, 1100)
