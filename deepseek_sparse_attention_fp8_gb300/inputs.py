@@ -102,18 +102,20 @@ def _e4m3_codes(x: np.ndarray) -> np.ndarray:
 def make_workload(name: str, seed: int | None = None, *, B: int | None = None, L=None, q_len: int | None = None,
                   index_topk: int | None = None, ld_pad: int = 128, lens=None, block_size: int = 64,
                   q_std: float = 1.0, kv_fp8: bool = False, Hi: int | None = None, Di: int | None = None,
-                  q_lens=None) -> Workload:
+                  q_lens=None, H: int | None = None) -> Workload:
     """Build one of the named workloads (optionally overriding a few sizes
     for smaller parity cases). `lens` gives explicit per-request lengths and
     `q_lens` per-request query counts (with `lens`, one entry per request);
     `q_std` the standard deviation of the MLA queries (1 in every workload);
     `kv_fp8` also lays the latent rows out as an fp8 latent cache; `Hi` and
-    `Di` change the indexer's head count and head dim."""
+    `Di` change the indexer's head count and head dim, `H` the MLA head count."""
     spec = dict(WORKLOADS[name])
     if Hi is not None:
         spec["Hi"] = Hi
     if Di is not None:
         spec["Di"] = Di
+    if H is not None:
+        spec["H"] = H
     if B is not None:
         spec["B"] = B
     if L is not None:

@@ -155,6 +155,22 @@ def test_other_block_sizes(base, kw, bs):
     check_attention(step.out.float().cpu().numpy(), ref, np.arange(wl.T), step.lse.cpu().numpy(), ref_lse)
 
 
+@pytest.mark.parametrize("H", [16, 64, 100])
+@pytest.mark.parametrize("splits", [1, 2])
+def test_fewer_mla_heads(H, splits):
+    """MLA head counts below the kernel's 128 rows (16 per GPU is DeepSeek's
+    128 under 8-way tensor parallelism; 100 is not a multiple of 16): the
+    attention against the oracle, split and unsplit."""
+    wl = make_workload("decode_b32_l8192", H=H, index_topk=512, lens=[3000, 1111, 200])
+    step = DsaStep(wl, num_kv_splits=splits)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) == 0
+    idx = step.topk_idx.cpu().numpy()
+    ref, ref_lse = oracle_attention(wl, idx)
+    check_attention(step.out.float().cpu().numpy(), ref, np.arange(wl.T), step.lse.cpu().numpy(), ref_lse)
+
+
 @pytest.mark.parametrize("K", [100, 2047])
 def test_unpadded_logits_rows_and_odd_topk(K):
     """Logits rows exactly as long as the longest request (ld = 2999, not a
