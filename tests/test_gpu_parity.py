@@ -171,6 +171,29 @@ def test_fewer_mla_heads(H, splits):
     check_attention(step.out.float().cpu().numpy(), ref, np.arange(wl.T), step.lse.cpu().numpy(), ref_lse)
 
 
+@pytest.mark.parametrize("kv_fp8", [False, True])
+@pytest.mark.parametrize("H", [16, 100])
+def test_fewer_mla_heads_prefill_entry(H, kv_fp8):
+    """Fewer MLA heads through the prefill entry point (a batch of up to three
+    query tokens per request) and over the fp8 latent cache."""
+    wl = make_workload("mixed_b64_mtp2", H=H, index_topk=512, lens=[900, 5000, 65], q_lens=[3, 2, 1],
+                       kv_fp8=kv_fp8)
+    step = DsaStep(wl, kv_fp8=kv_fp8)
+    assert step.prefill
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) == 0
+    idx = step.topk_idx.cpu().numpy()
+    if kv_fp8:
+        q = bf16_bits_to_float(wl.q)
+        kv = O.mla_fp8_decode_cache(wl.kv_cache_fp8, wl.Dk, wl.Dv)
+        ref, ref_lse = O.sparse_mla(q, kv, wl.kv_block_stride, wl.block_table, wl.seq_lens, wl.query_start_loc, idx,
+                                    wl.softmax_scale, wl.Dv, wl.block_size)
+    else:
+        ref, ref_lse = oracle_attention(wl, idx)
+    check_attention(step.out.float().cpu().numpy(), ref, np.arange(wl.T), step.lse.cpu().numpy(), ref_lse)
+
+
 @pytest.mark.parametrize("K", [100, 2047])
 def test_unpadded_logits_rows_and_odd_topk(K):
     """Logits rows exactly as long as the longest request (ld = 2999, not a
