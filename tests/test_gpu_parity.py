@@ -194,6 +194,23 @@ def test_fewer_mla_heads_prefill_entry(H, kv_fp8):
     check_attention(step.out.float().cpu().numpy(), ref, np.arange(wl.T), step.lse.cpu().numpy(), ref_lse)
 
 
+@pytest.mark.parametrize("K,splits", [(4096, 0), (6000, 3), (6000, 8)])
+def test_index_topk_above_one_split(K, splits):
+    """index_topk above the 2048 slots one split may cover (automatic and
+    explicit split counts): the top-k exact and the attention against the
+    oracle."""
+    wl = make_workload("decode_b32_l8192", index_topk=K, lens=[9000, 5000, 700])
+    step = DsaStep(wl, num_kv_splits=splits)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) == 0
+    got = step.logits.cpu().numpy()
+    idx = step.topk_idx.cpu().numpy()
+    check_topk_sets(idx, O.topk(got, wl.seq_lens, wl.query_start_loc, wl.index_topk), range(wl.T))
+    ref, ref_lse = oracle_attention(wl, idx)
+    check_attention(step.out.float().cpu().numpy(), ref, np.arange(wl.T), step.lse.cpu().numpy(), ref_lse)
+
+
 @pytest.mark.parametrize("K", [100, 2047])
 def test_unpadded_logits_rows_and_odd_topk(K):
     """Logits rows exactly as long as the longest request (ld = 2999, not a
